@@ -1,0 +1,446 @@
+"""CPU oracle for the DDP gradient-synchronisation hot path.
+
+TEST INFRASTRUCTURE ONLY.  This module is the plain, slow, obviously-correct
+definition that the CUDA path is checked against.  Only the test suite, the
+smoke check and the benchmark's CPU-baseline leg may import it; the product
+library never calls it and has no CPU fallback.  It shares no code, table or
+constant generator with the CUDA sources.
+
+Sources (web pages; section numbers are the pages' own):
+  [TR24]  Tech-Renaissance, "(24) NCCL通信与分布式数据并行"
+  [TR16]  Tech-Renaissance, "(16) DTensor"
+  [DDP]   AI_Infra notes, "1.DataParallel / DDP" (sgdbs.github.io)
+Each function names the section it follows.  Where the pages are silent the
+reading taken is stated in the docstring.
+
+Precision: the gradient average, the 1/N scale and the SGD step are fp32 as on
+the pages ([TR24] §一 says the local gradients are FP32; [TR24] §九 scales with
+a float reciprocal).  Every fp32 operation below is a separate numpy ufunc on
+float32 arrays, i.e. one IEEE round-to-nearest-even per operation, no fused
+multiply-add.  SyncBatchNorm statistics, which no page fixes, are fp64.
+
+Parity pins: every function here is pinned by tests/test_oracle_*.py against
+facts that do not come from this file (worked examples, closed forms,
+invariants, brute force, independent library routines).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# bf16 <-> fp32
+# ---------------------------------------------------------------------------
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to fp32: the bf16 pattern
+    is the top half of the fp32 pattern.  This is the "AMP grad cast" that the
+    n_cdg / n_cfg graphs of [TR24] §十一 perform before the all-reduce."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def f64_to_bf16_rne(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to bf16 (nearest, ties to even) directly from the
+    fp64 value, returned as fp64 holding the bf16 value.  Used to state the
+    expected bf16 outputs of SyncBatchNorm; finite inputs only."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros_like(x)
+    nz = x != 0
+    m, e = np.frexp(x[nz])          # x = m * 2**e, 0.5 <= |m| < 1
+    # bf16 has 8 significant bits: scale the mantissa to [128, 256)
+    sig = m * 256.0
+    r = np.round(sig)               # numpy rounds half to even
+    out[nz] = np.ldexp(r, e - 8)
+    return out
+
+
+def _as_f32(g: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "f32":
+        return np.ascontiguousarray(g, dtype=np.float32)
+    if dtype == "bf16":
+        return bf16_bits_to_f32(g)
+    if dtype == "f64":
+        return np.ascontiguousarray(g, dtype=np.float64)
+    if dtype == "obj":              # symbolic values (object arrays), for order checks
+        return np.asarray(g, dtype=object)
+    raise ValueError(dtype)
+
+# ---------------------------------------------------------------------------
+# gradient averaging  ([TR24] §一, §九; [DDP] §4.2)
+# ---------------------------------------------------------------------------
+
+
+def grad_mean(grads, dtype: str = "f32") -> np.ndarray:
+    """grad_sync = zeros; for r in 0..N-1: grad_sync += grad[r]; grad_sync /= N.
+
+    [TR24] §一 gives exactly this loop; [DDP] §4.2 sums with an all-reduce and
+    then divides by world_size.  The accumulator starts at +0, replicas are
+    added in rank order, each addition rounds to the accumulator's precision,
+    and the final step is a true division by float(N).  ``dtype`` names how the
+    replica arrays are stored: "f32", "bf16" (uint16 bit patterns, widened
+    exactly before the sum) or "f64" (used by the data-parallel identity
+    check, where the same loop runs in fp64)."""
+    n = len(grads)
+    if n < 1:
+        raise ValueError("need at least one replica")
+    first = _as_f32(grads[0], dtype)
+    acc = np.zeros(first.shape, dtype=first.dtype)
+    for r in range(n):
+        acc = acc + _as_f32(grads[r], dtype)
+    return acc / first.dtype.type(n)
+
+
+def grad_mean_tree(grads, dtype: str = "f32") -> np.ndarray:
+    """Pairwise (binary-tree) order of the same average, for a power-of-two
+    replica count: level by level, neighbours (2i, 2i+1) are added, then the
+    total is divided by N.  Tree all-reduce is described in [DDP] §2.13 and
+    [TR24] §二; only the summation order differs from grad_mean (the tree has
+    no +0 start: the first addition is g0 + g1)."""
+    n = len(grads)
+    if n < 1 or (n & (n - 1)) != 0:
+        raise ValueError("tree order needs a power-of-two replica count")
+    level = [_as_f32(g, dtype) for g in grads]
+    while len(level) > 1:
+        level = [level[2 * i] + level[2 * i + 1] for i in range(len(level) // 2)]
+    return level[0] / level[0].dtype.type(n)
+
+
+def ring_allreduce_mean(grads, dtype: str = "f32"):
+    """The average as a ring all-reduce produces it, chunk by chunk.
+
+    [DDP] §2.10-2.11: the flat buffer is cut into N chunks (chunk j = the j-th
+    of N near-equal contiguous pieces, the first numel % N pieces one element
+    longer).  During reduce-scatter the partial sum of chunk j starts at the
+    GPU that owns chunk j (A_jj), travels to GPU j+1, j+2, ... each of which
+    adds its own copy, so chunk j is summed in the order j, j+1, ..., j-1
+    (mod N) -- the order the page's 4-GPU tables show (σ_0 = ((A_00 + A_10) +
+    A_20) + A_30, σ_1 starts from A_11, ...).  The all-gather then copies σ_j
+    unchanged to every GPU, and the result is divided by N.
+
+    Returns (mean, chunk_bounds)."""
+    n = len(grads)
+    gs = [_as_f32(g, dtype) for g in grads]
+    numel = gs[0].shape[0]
+    base, rem = divmod(numel, n)
+    bounds = []
+    start = 0
+    for j in range(n):
+        ln = base + (1 if j < rem else 0)
+        bounds.append((start, start + ln))
+        start += ln
+    out = np.empty(numel, dtype=gs[0].dtype)
+    for j, (a, b) in enumerate(bounds):
+        acc = gs[j][a:b].copy()
+        for step in range(1, n):
+            acc = acc + gs[(j + step) % n][a:b]
+        out[a:b] = acc / gs[0].dtype.type(n)
+    return out, bounds
+
+# ---------------------------------------------------------------------------
+# SGD after the sync  ([DDP] §5.3 update rule; momentum / weight decay: reading)
+# ---------------------------------------------------------------------------
+
+
+def sgd_step(grads, theta: np.ndarray, buf, lr: float, momentum: float, weight_decay: float,
+             dtype: str = "f32"):
+    """One SGD step on the averaged gradient.
+
+    [DDP] §5.3 gives θ_{t+1} = θ_t − η g_t with g_t the averaged gradient, and
+    [DDP] §三 (3.1) says every rank runs the same deterministic step on the
+    same synced gradient.  The pages give no momentum or weight-decay formula;
+    the reading taken is PyTorch's SGD (dampening 0, no Nesterov), each fp32
+    operation rounded on its own, in this order:
+
+        g = grad_mean(grads)
+        d = g + wd*θ            (only if wd != 0)
+        b = μ*buf + d; buf = b; d = b   (only if μ != 0; buf starts at zero)
+        θ = θ − lr*d
+
+    Returns (theta_new, buf_new_or_None, g)."""
+    f = np.float32
+    g = grad_mean(grads, dtype)
+    th = np.ascontiguousarray(theta, dtype=np.float32)
+    d = g
+    if weight_decay != 0.0:
+        d = d + f(weight_decay) * th
+    b_new = None
+    if momentum != 0.0:
+        b_new = f(momentum) * np.ascontiguousarray(buf, dtype=np.float32) + d
+        d = b_new
+    th_new = th - f(lr) * d
+    return th_new, b_new, g
+
+# ---------------------------------------------------------------------------
+# bucket planning  ([DDP] §3.2 and §4.2; [TR24] §三, §八; [TR16] §四, §六)
+# ---------------------------------------------------------------------------
+
+PLAN_CAP = 0
+PLAN_DEEP_FIRST = 1
+
+
+def plan_buckets(numels, elem_bytes: int, cap_bytes: int, mode: int = PLAN_CAP,
+                 is_first=None, align_bytes: int = 256):
+    """Partition a model's gradient tensors into flat buckets.
+
+    PLAN_CAP ([DDP] §4.2: ``params_in_reverse = list(params)[::-1]`` then
+    ``_build_buckets(..., bucket_size_mb=25)``; [DDP] §3.2: buckets follow
+    the reverse of registration order because backward produces the last
+    layer's gradient first).  ``_build_buckets`` itself is not given; the
+    reading is the greedy fill: walk tensors last-registered first, and close
+    the open bucket before a tensor whose bytes would push it past the cap.  A
+    tensor larger than the cap ends up alone in its bucket.
+
+    PLAN_DEEP_FIRST ([TR24] §八): exactly two buckets, DEEP first (its
+    all-reduce overlaps the first layers' backward), then FIRST.  Tensors with
+    ``is_first`` true go to FIRST, the rest to DEEP, each in reverse
+    registration order.  No cap applies.  An empty group gives no bucket.
+
+    Layout ([TR16] §四 MemoryPlan::finalize, §六 align_up_256): buckets are
+    laid out one after another in one flat buffer; tensors are packed without
+    gaps inside a bucket; each bucket's base offset is rounded up to
+    ``align_bytes``.
+
+    Returns a dict with
+      buckets: list of (offset_elems, numel, first, count) where first/count
+               index into ``order``;
+      order: tensor ids in flat-buffer order;
+      tensor_offset: element offset of each tensor id;
+      tensor_bucket: bucket index of each tensor id;
+      total_elems: flat buffer length (end of the last bucket, aligned)."""
+    T = len(numels)
+    if align_bytes % elem_bytes != 0:
+        raise ValueError("align_bytes must be a multiple of elem_bytes")
+    align = align_bytes // elem_bytes
+    groups = []
+    if mode == PLAN_CAP:
+        cur, cur_bytes = [], 0
+        for t in reversed(range(T)):
+            nb = numels[t] * elem_bytes
+            if cur and cur_bytes + nb > cap_bytes:
+                groups.append(cur)
+                cur, cur_bytes = [], 0
+            cur.append(t)
+            cur_bytes += nb
+        if cur:
+            groups.append(cur)
+    elif mode == PLAN_DEEP_FIRST:
+        deep = [t for t in reversed(range(T)) if not is_first[t]]
+        first = [t for t in reversed(range(T)) if is_first[t]]
+        groups = [g for g in (deep, first) if g]
+    else:
+        raise ValueError("unknown mode")
+
+    buckets, order = [], []
+    tensor_offset = [0] * T
+    tensor_bucket = [0] * T
+    cursor = 0
+    for bi, grp in enumerate(groups):
+        off = cursor
+        pos = off
+        first_idx = len(order)
+        for t in grp:
+            tensor_offset[t] = pos
+            tensor_bucket[t] = bi
+            pos += numels[t]
+            order.append(t)
+        buckets.append((off, pos - off, first_idx, len(grp)))
+        cursor = -(-pos // align) * align
+    return {"buckets": buckets, "order": order, "tensor_offset": tensor_offset,
+            "tensor_bucket": tensor_bucket, "total_elems": cursor}
+
+# ---------------------------------------------------------------------------
+# SyncBatchNorm merge + apply  ([DDP] §4.3; [TR24] §三, §十二)
+# ---------------------------------------------------------------------------
+
+
+def syncbn(xs, eps: float = 1e-5, gamma=None, beta=None, dtype: str = "bf16"):
+    """Strict SyncBatchNorm forward over N replicas' activations [B, C, H, W].
+
+    [TR24] §十二: strict SyncBatchNorm all-reduces every rank's per-channel
+    sum and sum of squares before the BN finalize/apply; [DDP] §4.3: the
+    statistics then cover the whole global batch.  In fp64:
+        s_r[c] = Σ x_r[:, c], q_r[c] = Σ x_r[:, c]^2, n_r = B*H*W
+        S = Σ_r s_r, Q = Σ_r q_r, M = Σ_r n_r
+        mean = S / M,  var = Q / M − mean^2  (biased, as BN normalises with)
+        invstd = 1 / sqrt(var + eps)
+        y_r = (x_r − mean) * invstd * γ + β
+    γ defaults to 1 and β to 0 (the pages give neither).
+    Returns (mean[C], invstd[C], [y_r]) all fp64."""
+    xs64 = []
+    for x in xs:
+        x = np.asarray(x)
+        xs64.append(bf16_bits_to_f32(x).astype(np.float64) if dtype == "bf16"
+                    else np.asarray(x, dtype=np.float64))
+    C = xs64[0].shape[1]
+    S = np.zeros(C)
+    Q = np.zeros(C)
+    M = 0
+    for x in xs64:
+        S += x.sum(axis=(0, 2, 3))
+        Q += (x * x).sum(axis=(0, 2, 3))
+        M += x.shape[0] * x.shape[2] * x.shape[3]
+    mean = S / M
+    var = Q / M - mean * mean
+    invstd = 1.0 / np.sqrt(var + eps)
+    g = np.ones(C) if gamma is None else np.asarray(gamma, dtype=np.float64)
+    b = np.zeros(C) if beta is None else np.asarray(beta, dtype=np.float64)
+    ys = [(x - mean[None, :, None, None]) * invstd[None, :, None, None] * g[None, :, None, None]
+          + b[None, :, None, None] for x in xs64]
+    return mean, invstd, ys
+
+
+def syncbn_stats_at(xs, c: int, eps: float = 1e-5, dtype: str = "bf16"):
+    """mean and invstd of one channel only (same definition as ``syncbn``),
+    for spot checks on full-size inputs."""
+    S = Q = 0.0
+    M = 0
+    for x in xs:
+        v = np.asarray(x)[:, c]
+        v = bf16_bits_to_f32(v).astype(np.float64) if dtype == "bf16" else v.astype(np.float64)
+        S += v.sum()
+        Q += (v * v).sum()
+        M += v.size
+    mean = S / M
+    var = Q / M - mean * mean
+    return mean, 1.0 / math.sqrt(var + eps)
+
+# ---------------------------------------------------------------------------
+# DistributedSampler  ([DDP] §4.4)
+# ---------------------------------------------------------------------------
+
+_M64 = (1 << 64) - 1
+SPLITMIX_GAMMA = 0x9E3779B97F4A7C15
+FEISTEL_ROUNDS = 4
+WALK_CAP = 4096
+
+
+def splitmix64_mix(z: int) -> int:
+    """The SplitMix64 output function (Steele, Lea & Flood, "Fast splittable
+    pseudorandom number generators", OOPSLA 2014), on Python ints mod 2^64."""
+    z &= _M64
+    z ^= z >> 30
+    z = (z * 0xBF58476D1CE4E5B9) & _M64
+    z ^= z >> 27
+    z = (z * 0x94D049BB133111EB) & _M64
+    return z ^ (z >> 31)
+
+
+def splitmix64_stream(state: int, count: int):
+    """First ``count`` outputs of SplitMix64 seeded with ``state``: the state
+    advances by the golden-ratio increment before each output."""
+    out = []
+    for _ in range(count):
+        state = (state + SPLITMIX_GAMMA) & _M64
+        out.append(splitmix64_mix(state))
+    return out
+
+
+def _feistel_params(n: int):
+    bits = max(1, (n - 1).bit_length())      # smallest bits with 2^bits >= n
+    h = (bits + 1) // 2
+    return h, (1 << h) - 1
+
+
+def feistel_encrypt(x: int, key: int, n: int) -> int:
+    """One pass of the keyed balanced Feistel network on 2h bits, where h is
+    half of ceil(log2 n) rounded up.  Round keys are the first four SplitMix64
+    outputs from state ``key``; round i maps (L, R) -> (R, L xor
+    (mix64(R xor k_i) mod 2^h)).  Any round function gives a bijection."""
+    h, mask = _feistel_params(n)
+    rk = splitmix64_stream(key, FEISTEL_ROUNDS)
+    L, R = x >> h, x & mask
+    for i in range(FEISTEL_ROUNDS):
+        L, R = R, L ^ (splitmix64_mix(R ^ rk[i]) & mask)
+    return (L << h) | R
+
+
+def keyed_perm(j: int, key: int, n: int) -> int:
+    """π_key(j) for j in [0, n): Feistel encryption with cycle walking (encrypt
+    again while the value is >= n).  Returns -1 if the walk exceeds WALK_CAP
+    encryptions (never observed; both sides report it as an error).
+
+    [DDP] §4.4 shuffles with torch.randperm(n, generator seeded with
+    seed+epoch).  torch's generator stream is not reproducible outside torch,
+    so the reading is: any permutation keyed by seed+epoch that every rank
+    computes identically; this keyed Feistel permutation is the one used."""
+    if n <= 1:
+        return j
+    y = feistel_encrypt(j, key, n)
+    steps = 1
+    while y >= n:
+        if steps >= WALK_CAP:
+            return -1
+        y = feistel_encrypt(y, key, n)
+        steps += 1
+    return y
+
+
+def keyed_perm_all(key: int, n: int) -> np.ndarray:
+    """π_key(0..n-1) for every index, numpy-vectorised version of keyed_perm
+    (same arithmetic on uint64 lanes; wrapping multiplication mod 2^64)."""
+    if n <= 1:
+        return np.arange(n, dtype=np.int64)
+    h, mask = _feistel_params(n)
+    rk = [np.uint64(k) for k in splitmix64_stream(key, FEISTEL_ROUNDS)]
+    m = np.uint64(mask)
+    hh = np.uint64(h)
+
+    def mix(z):
+        z = z ^ (z >> np.uint64(30))
+        z = z * np.uint64(0xBF58476D1CE4E5B9)
+        z = z ^ (z >> np.uint64(27))
+        z = z * np.uint64(0x94D049BB133111EB)
+        return z ^ (z >> np.uint64(31))
+
+    def enc(x):
+        L, R = x >> hh, x & m
+        for i in range(FEISTEL_ROUNDS):
+            L, R = R, L ^ (mix(R ^ rk[i]) & m)
+        return (L << hh) | R
+
+    with np.errstate(over="ignore"):
+        y = enc(np.arange(n, dtype=np.uint64))
+        steps = 1
+        todo = y >= np.uint64(n)
+        while todo.any():
+            if steps >= WALK_CAP:
+                raise RuntimeError("cycle walk exceeded its cap")
+            y[todo] = enc(y[todo])
+            steps += 1
+            todo = y >= np.uint64(n)
+    return y.astype(np.int64)
+
+
+def sampler_num_samples(n: int, n_replicas: int, drop_last: bool) -> int:
+    """[DDP] §4.4: floor(n/N) with drop_last, else ceil(n/N)."""
+    return n // n_replicas if drop_last else -(-n // n_replicas)
+
+
+def dist_sampler_indices(n: int, n_replicas: int, rank: int, seed: int, epoch: int,
+                         shuffle: bool = True, drop_last: bool = False) -> np.ndarray:
+    """The indices rank ``rank`` draws in epoch ``epoch`` ([DDP] §4.4).
+
+        num_samples = drop_last ? n // N : ceil(n / N);  total = num_samples * N
+        base = shuffle ? π_{seed+epoch}(0..n-1) : 0..n-1
+        padded: base extended by repeating from its head up to total
+                (drop_last: base cut to total)
+        out = padded[rank : total : N]
+
+    ``rank`` = -1 returns every rank's list stacked rank-major [N, num_samples].
+    Padding repeats the head cyclically (padded[j] = base[j mod n]); that is
+    the page's ``indices += indices[:total-len]`` whenever total - n <= n,
+    which holds whenever n >= N - 1."""
+    ns = sampler_num_samples(n, n_replicas, drop_last)
+    total = ns * n_replicas
+    key = (seed + epoch) & _M64
+    base = keyed_perm_all(key, n) if shuffle else np.arange(n, dtype=np.int64)
+    if total == 0:
+        padded = np.zeros(0, dtype=np.int64)
+    else:
+        padded = base[np.arange(total, dtype=np.int64) % n]
+    if rank >= 0:
+        return padded[rank:total:n_replicas].copy()
+    return np.stack([padded[r:total:n_replicas] for r in range(n_replicas)]) if n_replicas else padded
