@@ -1,0 +1,523 @@
+#!/usr/bin/env python
+"""Benchmark of the bucketed N-replica gradient average on GB300.
+
+Headline workload (one "step" = one pass of the gradient-sync hot path):
+ResNet-50 parameter layout (161 tensors, 25,557,032 fp32 elements), 8
+replicas' gradients resident in HBM, planned into 25 MiB buckets in reverse
+registration order (5 buckets), each bucket averaged by one
+ddp_bucket_allreduce_mean launch.  Each bucket's launch is captured once as
+its own CUDA Graph on a side stream (as per-bucket communication graphs are
+captured once and replayed); a step replays the 5 graphs.
+
+Metric: algorithmic HBM bytes moved per second, (N+1)*4 bytes per element
+(N replica reads + one fp32 write), and that rate as a fraction of the
+measured HBM copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank runs its own copy of the workload on its
+own GPU (replicas only — the single-GPU path has no cross-GPU exchange), the
+timed region is bracketed by barriers, and the slowest rank's time is used.
+--impl reference times the CPU oracle (the plain numpy definition) on the host
+cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+MiB = 1 << 20
+N_REPLICAS = 8
+CAP_BYTES = 25 * MiB
+METRIC = "bucket allreduce-mean GB/s (HBM bytes moved) & % of HBM roofline, 1×GB300"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 10 ** 6
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=4000)
+    p.add_argument("--warmup", type=int, default=200)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-rows", action="store_true", help="skip the SGD / SyncBN / sampler rows")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- environment
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock, power and throttle reasons while a
+    region runs; samples are kept with their host timestamps."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append({"t": ts, "sm": float(parts[2]), "sm_max": float(parts[3]),
+                             "power": float(parts[4]) if parts[4] not in ("[N/A]", "N/A") else None,
+                             "hw_slowdown": parts[6], "hw_thermal": parts[7], "sw_thermal": parts[8],
+                             "sw_power_cap": parts[9]})
+            except ValueError:
+                continue
+        return rows
+
+
+def summarize_clocks(rows, t0, t1):
+    inside = [r for r in rows if t0 <= r["t"] <= t1]
+    window = "timed region"
+    if not inside:       # region shorter than the sampling period: nearest samples around it
+        inside = sorted(rows, key=lambda r: min(abs(r["t"] - t0), abs(r["t"] - t1)))[:3]
+        window = "nearest samples to a short timed region"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "no samples"}
+    reasons = set()
+    for r in inside:
+        for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power_cap", "sw_power_cap")):
+            if r[key].lower().startswith("active"):
+                reasons.add(name)
+    pw = [r["power"] for r in inside if r["power"] is not None]
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["sm_max"] for r in inside),
+            "reasons": sorted(reasons), "samples": len(inside), "window": window,
+            "power_w_max": max(pw) if pw else None}
+
+
+def profile_traffic(source_files):
+    """ncu DRAM bytes per launch of the dominant kernel, from the committed
+    summary, if the kernel's sources still hash to what was profiled."""
+    path = os.path.join(ROOT, "profiles", "mean_kernel_resnet50.md")
+    try:
+        txt = open(path, encoding="utf-8").read()
+    except OSError:
+        return None, None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source_sha256:\s*([0-9a-f]+)", txt)
+    if not m:
+        return None, None
+    h = hashlib.sha256()
+    for f in source_files:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest()[:16] != m.group(2)[:16]:
+        return None, "kernel changed since the ncu capture"
+    return float(m.group(1)), None
+
+
+def kernel_source_hash():
+    csrc = os.path.join(ROOT, "gradient_sync_ddp_gb300", "csrc")
+    return [os.path.join(csrc, f) for f in ("allreduce.cu", "common.cuh")]
+
+
+# ----------------------------------------------------------------------------- workload
+
+def resnet50_plan(plan_fn):
+    import workloads
+    num = workloads.numels(workloads.resnet50_layout())
+    return num, plan_fn(num, 4, CAP_BYTES)
+
+
+def algorithmic_bytes(plan, n=N_REPLICAS):
+    return sum((n + 1) * 4 * b[1] for b in plan["buckets"])
+
+
+def cpu_oracle_rate(plan, budget_s: float, seed_base: int = 0):
+    """Time the oracle's rank-ordered average on the host over a bounded
+    sample of the workload: the first k elements of every bucket, k chosen
+    so that the timed passes take about budget_s seconds."""
+    import numpy as np
+
+    import oracle
+    gen = np.random.Generator(np.random.PCG64(1234 + 200 + seed_base))
+    probe = 1 << 18
+    reps = [(gen.standard_normal(probe, dtype=np.float32) * np.float32(0.01)) for _ in range(N_REPLICAS)]
+    t = time.perf_counter()
+    oracle.grad_mean(reps)
+    per_elem = max((time.perf_counter() - t) / probe, 1e-10)
+    full = max(b[1] for b in plan["buckets"])
+    k = int(min(full, max(probe, budget_s / per_elem / len(plan["buckets"]) / 3)))
+    data = [[(gen.standard_normal(min(k, b[1]), dtype=np.float32) * np.float32(0.01)) for _ in range(N_REPLICAS)]
+            for b in plan["buckets"]]
+    elems = sum(len(d[0]) for d in data)
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        for d in data:
+            oracle.grad_mean(d)
+        passes += 1
+        if time.perf_counter() - t0 >= budget_s or passes >= 1000:
+            break
+    dt = time.perf_counter() - t0
+    nbytes = (N_REPLICAS + 1) * 4 * elems * passes
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {k:,} elements of each of the {len(plan['buckets'])} buckets x {N_REPLICAS} "
+                      f"replicas ({elems:,} elements per pass), {passes} passes in {dt:.1f} s, numpy "
+                      f"single-threaded on {os.cpu_count()} host cores"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import oracle
+    import workloads
+    num, plan = resnet50_plan(oracle.plan_buckets)
+    nb = len(plan["buckets"])
+    gen = np.random.Generator(np.random.PCG64(1234 + 200))
+    probe = 1 << 18
+    reps = [(gen.standard_normal(probe, dtype=np.float32) * np.float32(0.01)) for _ in range(N_REPLICAS)]
+    t = time.perf_counter()
+    oracle.grad_mean(reps)
+    per_elem = max((time.perf_counter() - t) / probe, 1e-10)
+    budget = 120.0 / max(1, args.steps + args.warmup)          # whole run: about two minutes
+    k = int(min(max(b[1] for b in plan["buckets"]), max(4096, budget / per_elem / nb)))
+    data = [[workloads.normal_f32(workloads.rng(2, r), min(k, b[1]), 0.0, 0.01) for r in range(N_REPLICAS)]
+            for b in plan["buckets"]]
+    elems = sum(len(d[0]) for d in data)
+    for _ in range(args.warmup):
+        for d in data:
+            oracle.grad_mean(d)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for d in data:
+            oracle.grad_mean(d)
+    dt = time.perf_counter() - t0
+    value = (N_REPLICAS + 1) * 4 * elems * args.steps / dt / 1e9
+    sample = (f"each step: first {k:,} elements of each of the {nb} buckets x {N_REPLICAS} replicas "
+              f"({elems:,} elements), numpy single-threaded")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / max(1, args.steps) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic: seeded N(0, 0.01) fp32 replica gradients (numpy PCG64)",
+            "config": workload_config(plan, num),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(plan, num):
+    return {"workload": "ResNet-50 parameter layout (161 tensors, 25,557,032 fp32 elements), 8 replicas, "
+                        "25 MiB buckets in reverse registration order, rank-ordered mean",
+            "replicas": N_REPLICAS, "tensors": len(num), "elements": sum(num), "buckets": len(plan["buckets"]),
+            "bucket_cap_mib": 25, "bytes_per_step": algorithmic_bytes(plan),
+            "l2": "inputs larger than L2 (818 MB of replica gradients read per step vs 129 MB L2); no flush",
+            "parallelism": "replicas only: each GPU averages its own 8 resident replicas"}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import workloads
+    from gradient_sync_ddp_gb300 import build as _b
+    _b.build()
+    import gradient_sync_ddp_gb300 as g
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    num, plan = resnet50_plan(g.ddp_plan_buckets)
+    total = plan["total_elems"]
+    buckets = plan["buckets"]
+    reps = [workloads.device_normal((total,), 0.0, 0.01, workloads.seed_for(2, r) + 1000 * rank, device=dev)
+            for r in range(N_REPLICAS)]
+    out = torch.empty(total, device=dev)
+    side = torch.cuda.Stream(device=dev)
+
+    def launch(b):
+        off, n = buckets[b][0], buckets[b][1]
+        g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps], out[off:off + n])
+
+    # capture one graph per bucket on the side stream
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for b in range(len(buckets)):
+            launch(b)
+    torch.cuda.synchronize()
+    graphs = []
+    for b in range(len(buckets)):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=side):
+            launch(b)
+        graphs.append(gr)
+    torch.cuda.synchronize()
+
+    step_bytes = algorithmic_bytes(plan)
+    bucket_bytes = [(N_REPLICAS + 1) * 4 * b[1] for b in buckets]
+    nb = len(graphs)
+    K, W = args.steps, args.warmup
+
+    with torch.cuda.stream(side):
+        for _ in range(W):
+            for gr in graphs:
+                gr.replay()
+    torch.cuda.synchronize()
+
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(K * nb + 1)]
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    with torch.cuda.stream(side):
+        events[0].record()
+        i = 1
+        for _ in range(K):
+            for gr in graphs:
+                gr.replay()
+                events[i].record()
+                i += 1
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clock_rows = sampler.stop() if rank == 0 else []
+    elapsed_ms = events[0].elapsed_time(events[-1])
+    dur = [events[j].elapsed_time(events[j + 1]) for j in range(K * nb)]   # per launch, ms
+    elapsed = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(elapsed.item())
+    value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
+
+    # per-launch roofline of the averaging kernel over the timed region
+    sum_dur = [0.0] * nb
+    for j, d in enumerate(dur):
+        sum_dur[j % nb] += d
+    achieved = sum(bucket_bytes) * K / (sum(sum_dur) * 1e-3) / 1e9
+    peak, peak_kind = load_peak()
+    traffic, traffic_note = profile_traffic(kernel_source_hash())
+
+    # end to end through the public API: pinned host replicas -> HBM, 5 bucket calls, result -> pinned host
+    host_reps = [torch.empty(total, dtype=torch.float32, pin_memory=True) for _ in range(N_REPLICAS)]
+    for h, d in zip(host_reps, reps):
+        h.copy_(d)
+    host_out = torch.empty(total, dtype=torch.float32, pin_memory=True)
+    torch.cuda.synchronize()
+
+    def e2e_step():
+        for h, d in zip(host_reps, reps):
+            d.copy_(h, non_blocking=True)
+        for b in range(nb):
+            launch(b)
+        host_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(side):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        e0.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = world * step_bytes * args.e2e_steps / (float(e2e_ms.item()) * 1e-3) / 1e9
+
+    rows = None
+    if rank == 0 and world == 1 and not args.no_rows:
+        del host_reps, host_out
+        rows = bench_rows(g, torch, dev, peak, peak_kind)
+
+    if rank == 0:
+        cpu = None if args.no_cpu_baseline or world > 1 else cpu_oracle_rate(plan, args.cpu_seconds)
+        clocks = summarize_clocks(clock_rows, t_host0, t_host1)
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic: seeded N(0, 0.01) fp32 replica gradients drawn on the device",
+            "config": workload_config(plan, num),
+            "hbm_fraction": value / world / peak,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} (HBM copy bandwidth)",
+                         "kernel": "mean_kernel (ddp_bucket_allreduce_mean, fp32, rank order, N=8)",
+                         "bytes_per_launch": bucket_bytes,
+                         "avg_launch_us": [s / K * 1e3 for s in sum_dur],
+                         **({"traffic_note": traffic_note} if traffic_note else {})},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": N_REPLICAS * total * 4,
+                    "d2h_bytes_per_step": total * 4, "steps": args.e2e_steps},
+            "gpu_launches": K * nb,
+            "clocks": clocks,
+        }
+        if rows is not None:
+            line["rows"] = rows
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def _time_launches(torch, fn, iters, stream):
+    """Mean device time (ms) of fn() over iters launches on stream, after 3 warm-ups."""
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record()
+        for _ in range(iters):
+            fn()
+        b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def bench_rows(g, torch, dev, peak, peak_kind):
+    """The other rows of the hot path, each on its own workload (not part of
+    the headline value): fused SGD on GPT-2 small, SyncBN on the four
+    activation shapes, the ImageNet-size sampler, and the bf16 average."""
+    import workloads
+    side = torch.cuda.Stream(device=dev)
+    rows = {}
+
+    # fused SGD, GPT-2 small DEEP/FIRST, bf16 grads, momentum 0.9, wd 1e-4
+    layout, first = workloads.gpt2_small_layout()
+    num = workloads.numels(layout)
+    plan = g.ddp_plan_buckets(num, 2, 0, g.PLAN_DEEP_FIRST, first)
+    total = plan["total_elems"]
+    reps = [workloads.device_normal((total,), 0.0, 0.01, workloads.seed_for(3, r), device=dev,
+                                    dtype=torch.bfloat16) for r in range(N_REPLICAS)]
+    theta = workloads.device_normal((total,), 0.0, 0.02, workloads.seed_for(3, 99), device=dev)
+    buf = torch.zeros(total, device=dev)
+
+    def sgd_step():
+        for off, n, _, _ in plan["buckets"]:
+            g.ddp_bucket_allreduce_sgd([x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n],
+                                       0.1, 0.9, 1e-4)
+    ms = _time_launches(torch, sgd_step, 50, side)
+    nbytes = sum((2 * N_REPLICAS + 16) * b[1] for b in plan["buckets"])
+    rows["sgd_gpt2_small"] = {"workload": "GPT-2 small (124,439,808 params), 8 bf16 replicas, DEEP/FIRST buckets, "
+                                          "SGD momentum 0.9 wd 1e-4", "ms": ms, "bytes": nbytes,
+                              "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+
+    # bf16 -> fp32 average of the same buckets
+    outb = torch.empty(total, device=dev)
+
+    def mean_bf16():
+        for off, n, _, _ in plan["buckets"]:
+            g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps], outb[off:off + n])
+    ms = _time_launches(torch, mean_bf16, 50, side)
+    nbytes = sum((2 * N_REPLICAS + 4) * b[1] for b in plan["buckets"])
+    rows["mean_bf16_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, DEEP/FIRST, average to fp32",
+                                    "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
+                                    "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+    del reps, theta, buf, outb
+
+    # SyncBN, 4 shapes
+    for C, H, W in workloads.SYNCBN_SHAPES:
+        B = workloads.SYNCBN_BATCH
+        xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, workloads.seed_for(4, r), device=dev,
+                                      dtype=torch.bfloat16) for r in range(N_REPLICAS)]
+        ys = [torch.empty_like(x) for x in xs]
+        ws = torch.empty(g.syncbn_workspace_bytes(N_REPLICAS, B, C, H, W), dtype=torch.uint8, device=dev)
+        mean = torch.empty(C, device=dev)
+        inv = torch.empty(C, device=dev)
+        ms = _time_launches(torch, lambda: g.syncbn_merge_apply(xs, ys, mean, inv, ws), 30, side)
+        nbytes = 6 * N_REPLICAS * B * C * H * W
+        rows[f"syncbn_{C}x{H}x{W}"] = {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
+                                       "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+                                       "launches": 3,
+                                       "note": "inputs smaller than L2" if nbytes / 3 < L2_BYTES else ""}
+        del xs, ys
+
+    # sampler
+    n, N = workloads.SAMPLER_N_ITEMS, workloads.SAMPLER_REPLICAS
+    out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
+    ms = _time_launches(torch, lambda: g.dist_sampler_indices(n, N, -1, 0, 1, True, False, out), 100, side)
+    rows["sampler_imagenet"] = {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
+                                "Mindex_per_s": out.numel() / ms / 1e3, "bytes": out.numel() * 8,
+                                "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu", "launches": 1}
+    rows["_peak"] = {"hbm_gbs": peak, "source": peak_kind}
+    return rows
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

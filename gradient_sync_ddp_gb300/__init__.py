@@ -1,0 +1,242 @@
+"""Python binding of libddp_sync.so — argument marshalling only.
+
+Every function here has the name of a C entry point declared in
+include/ddp_sync.h and does nothing but turn torch tensors (or plain Python
+values) into the pointers and sizes the C ABI takes, call it, and raise
+``DdpError`` on a non-zero status.  All computation runs in the library's
+CUDA kernels (or, for the planner, its C++ host code).  There is no fallback:
+if the library is missing, importing this package raises.
+
+torch is used for device memory and streams only: a tensor argument must
+already live where the C function expects it (device tensors for device
+pointers), and calls are enqueued on ``torch.cuda.current_stream()`` unless a
+``stream`` is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libddp_sync.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libddp_sync.so is not built ({LIB_PATH}); run "
+                      "`python -m gradient_sync_ddp_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MAX_REPLICAS = 16
+F32, BF16 = 0, 1
+PLAN_CAP, PLAN_DEEP_FIRST = 0, 1
+FLAG_TREE_ORDER, FLAG_WRITE_BACK_ALL, FLAG_RING_ORDER = 1, 2, 4
+
+DDP_OK = 0
+DDP_ERR_INVALID_ARG = -1
+DDP_ERR_ALIGNMENT = -2
+DDP_ERR_CAPACITY = -3
+DDP_ERR_CUDA = -4
+DDP_ERR_UNSUPPORTED = -5
+DDP_ERR_TIMEOUT = -6
+
+
+class DdpBucket(ctypes.Structure):
+    _fields_ = [("offset_elems", ctypes.c_int64), ("numel", ctypes.c_int64),
+                ("first", ctypes.c_int32), ("count", ctypes.c_int32)]
+
+
+_c = ctypes
+_P = _c.c_void_p
+_lib.ddp_plan_buckets.argtypes = [_c.c_int32, _P, _c.c_int32, _c.c_int64, _c.c_int32, _P, _c.c_int32,
+                                  _P, _c.c_int32, _P, _P, _P, _P, _P]
+_lib.ddp_plan_buckets.restype = _c.c_int
+_lib.ddp_bucket_allreduce_mean.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int64, _P, _c.c_uint32, _P]
+_lib.ddp_bucket_allreduce_mean.restype = _c.c_int
+_lib.ddp_bucket_allreduce_sgd.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int64, _P, _P, _c.c_float,
+                                          _c.c_float, _c.c_float, _P, _c.c_uint32, _P]
+_lib.ddp_bucket_allreduce_sgd.restype = _c.c_int
+_lib.syncbn_workspace_bytes.argtypes = [_c.c_int32] * 5
+_lib.syncbn_workspace_bytes.restype = _c.c_size_t
+_lib.syncbn_merge_apply.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
+                                    _c.c_float, _P, _P, _P, _c.c_int32, _P, _P, _P, _c.c_size_t, _P]
+_lib.syncbn_merge_apply.restype = _c.c_int
+_lib.dist_sampler_num_samples.argtypes = [_c.c_int64, _c.c_int32, _c.c_int32]
+_lib.dist_sampler_num_samples.restype = _c.c_int64
+_lib.dist_sampler_indices.argtypes = [_c.c_int64, _c.c_int32, _c.c_int32, _c.c_uint64, _c.c_uint64, _c.c_int32,
+                                      _c.c_int32, _P, _c.c_int64, _P, _P, _P]
+_lib.dist_sampler_indices.restype = _c.c_int
+_lib.ddp_status_string.argtypes = [_c.c_int]
+_lib.ddp_status_string.restype = _c.c_char_p
+_lib.ddp_last_cuda_error.argtypes = []
+_lib.ddp_last_cuda_error.restype = _c.c_int
+_lib.ddp_sync_version.argtypes = []
+_lib.ddp_sync_version.restype = _c.c_char_p
+
+
+class DdpError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _lib.ddp_status_string(status).decode()
+        if status == DDP_ERR_CUDA:
+            msg += f" (cudaError {_lib.ddp_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+def _check(st: int, where: str) -> int:
+    if st != DDP_OK:
+        raise DdpError(st, where)
+    return st
+
+
+def status_string(status: int) -> str:
+    return _lib.ddp_status_string(status).decode()
+
+
+def version() -> str:
+    return _lib.ddp_sync_version().decode()
+
+
+def lib_handle():
+    """The loaded ctypes library (for tests that call the C ABI directly)."""
+    return _lib
+
+
+def _ptr(x):
+    """Device/host address of a tensor, an int address, or None -> NULL."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr_array(items):
+    arr = (ctypes.c_void_p * max(1, len(items)))()
+    for i, t in enumerate(items):
+        arr[i] = _ptr(t)
+    return arr
+
+
+# ---------------------------------------------------------------- planner
+
+def ddp_plan_buckets(numels, elem_bytes: int, cap_bytes: int, mode: int = PLAN_CAP, is_first=None,
+                     align_bytes: int = 256):
+    """Host planner (C++).  Returns a dict like the oracle's planner:
+    buckets [(offset_elems, numel, first, count)], order, tensor_offset,
+    tensor_bucket, total_elems."""
+    T = len(numels)
+    c_num = (ctypes.c_int64 * max(1, T))(*numels)
+    c_first = None
+    if is_first is not None:
+        c_first = (ctypes.c_uint8 * max(1, T))(*[1 if f else 0 for f in is_first])
+    order = (ctypes.c_int32 * max(1, T))()
+    toff = (ctypes.c_int64 * max(1, T))()
+    tbk = (ctypes.c_int32 * max(1, T))()
+    nb = ctypes.c_int32(0)
+    total = ctypes.c_int64(0)
+    cap = max(1, T)
+    while True:
+        bk = (DdpBucket * cap)()
+        st = _lib.ddp_plan_buckets(T, ctypes.addressof(c_num), elem_bytes, cap_bytes, mode,
+                                   ctypes.addressof(c_first) if c_first is not None else None, align_bytes,
+                                   ctypes.addressof(bk), cap, ctypes.addressof(nb), ctypes.addressof(order),
+                                   ctypes.addressof(toff), ctypes.addressof(tbk), ctypes.addressof(total))
+        if st == DDP_ERR_CAPACITY and nb.value > cap:
+            cap = nb.value
+            continue
+        _check(st, "ddp_plan_buckets")
+        break
+    return {"buckets": [(b.offset_elems, b.numel, b.first, b.count) for b in bk[:nb.value]],
+            "order": list(order[:T]), "tensor_offset": list(toff[:T]), "tensor_bucket": list(tbk[:T]),
+            "total_elems": total.value}
+
+
+# ---------------------------------------------------------------- all-reduce
+
+def ddp_bucket_allreduce_mean(replicas, out, flags: int = 0, numel=None, stream=None) -> None:
+    """out[:numel] = average of replicas[r][:numel] (fp32 or bf16 tensors on one device)."""
+    if not 1 <= len(replicas) <= MAX_REPLICAS:
+        raise ValueError("need 1..16 replicas")
+    n = int(numel if numel is not None else replicas[0].numel())
+    _check(_lib.ddp_bucket_allreduce_mean(_ptr_array(replicas), len(replicas), _dtype_code(replicas[0]), n,
+                                          _ptr(out), flags, _stream_ptr(stream)),
+           "ddp_bucket_allreduce_mean")
+
+
+def ddp_bucket_allreduce_sgd(replicas, param, momentum_buf, lr: float, momentum: float, weight_decay: float,
+                             grad_out=None, flags: int = 0, numel=None, stream=None) -> None:
+    """Average the replicas and apply SGD (momentum, weight decay) to param in place."""
+    if not 1 <= len(replicas) <= MAX_REPLICAS:
+        raise ValueError("need 1..16 replicas")
+    n = int(numel if numel is not None else replicas[0].numel())
+    _check(_lib.ddp_bucket_allreduce_sgd(_ptr_array(replicas), len(replicas), _dtype_code(replicas[0]), n,
+                                         _ptr(param), _ptr(momentum_buf), lr, momentum, weight_decay,
+                                         _ptr(grad_out), flags, _stream_ptr(stream)),
+           "ddp_bucket_allreduce_sgd")
+
+
+# ---------------------------------------------------------------- SyncBN
+
+def syncbn_workspace_bytes(n_replicas: int, batch: int, C: int, H: int, W: int) -> int:
+    return int(_lib.syncbn_workspace_bytes(n_replicas, batch, C, H, W))
+
+
+def syncbn_merge_apply(xs, ys, mean_out, invstd_out, workspace, eps: float = 1e-5, gamma=None, beta=None,
+                       stream=None) -> None:
+    """Strict SyncBatchNorm forward over replicas xs[r] ([B, C, H, W], NCHW)
+    into ys[r]; mean_out/invstd_out are float32 [C]; workspace is a uint8
+    device tensor of at least syncbn_workspace_bytes(...) bytes."""
+    B, C, H, W = xs[0].shape
+    _check(_lib.syncbn_merge_apply(_ptr_array(xs), len(xs), _dtype_code(xs[0]), B, C, H, W, eps,
+                                   _ptr(gamma), _ptr(beta), _ptr_array(ys), _dtype_code(ys[0]),
+                                   _ptr(mean_out), _ptr(invstd_out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream)),
+           "syncbn_merge_apply")
+
+
+# ---------------------------------------------------------------- sampler
+
+def dist_sampler_num_samples(n_items: int, n_replicas: int, drop_last: bool) -> int:
+    v = int(_lib.dist_sampler_num_samples(n_items, n_replicas, int(bool(drop_last))))
+    if v < 0:
+        raise DdpError(DDP_ERR_INVALID_ARG, "dist_sampler_num_samples")
+    return v
+
+
+def dist_sampler_indices(n_items: int, n_replicas: int, rank: int, seed: int, epoch: int, shuffle: bool,
+                         drop_last: bool, out, walk_status=None, stream=None) -> int:
+    """Fill out (int64 device tensor) with rank's indices, or all ranks'
+    rank-major when rank == -1.  Returns num_samples."""
+    ns = ctypes.c_int64(0)
+    _check(_lib.dist_sampler_indices(n_items, n_replicas, rank, seed & (2 ** 64 - 1), epoch & (2 ** 64 - 1),
+                                     int(bool(shuffle)), int(bool(drop_last)), _ptr(out),
+                                     0 if out is None else out.numel(), ctypes.addressof(ns), _ptr(walk_status),
+                                     _stream_ptr(stream)),
+           "dist_sampler_indices")
+    return ns.value
+
+
+__all__ = [
+    "ddp_plan_buckets", "ddp_bucket_allreduce_mean", "ddp_bucket_allreduce_sgd", "syncbn_workspace_bytes",
+    "syncbn_merge_apply", "dist_sampler_num_samples", "dist_sampler_indices", "DdpError", "status_string",
+    "version", "lib_handle", "F32", "BF16", "PLAN_CAP", "PLAN_DEEP_FIRST", "FLAG_TREE_ORDER",
+    "FLAG_WRITE_BACK_ALL", "FLAG_RING_ORDER", "MAX_REPLICAS",
+]

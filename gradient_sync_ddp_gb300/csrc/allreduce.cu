@@ -1,0 +1,419 @@
+// N-replica bucket average (the single-GPU form of the gradient all-reduce)
+// and the same average fused with the SGD step.
+//
+// Definition: Tech-Renaissance "(24) NCCL通信与分布式数据并行" §一 — grad_sync
+// starts at zero, grad[r] is added for r = 0..N-1, then divided by float(N);
+// §九 — the all-reduce sums and a scale kernel multiplies by 1/world_size
+// (here one pass: the replicas are read once, the average written once).
+// AI_Infra notes "1.DataParallel / DDP" §2.11 (ring order) and §2.13 (tree
+// order) give the alternative summation orders; §5.3 the SGD update.
+//
+// GB300 design: the kernel is HBM-bound ((N+1)*4 bytes per fp32 element), so
+// each thread streams one 16-byte vector from every replica (all N loads are
+// issued before the first add, N*16 bytes in flight per thread), keeps the
+// adds in the exact rank order with __fadd_rn (no contraction), and writes
+// the fp32 result with a streaming store.  The grid is a multiple of the SM
+// count (resident blocks per SM x SMs) and strides over the bucket.  The
+// replica pointers travel in a __grid_constant__ parameter block, so a
+// launch is self-contained and capturable into a CUDA Graph.
+#include <cstdint>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace ddp {
+namespace {
+
+struct RepPtrs {
+    const void* p[DDP_MAX_REPLICAS];
+};
+
+enum Order { kRank = 0, kTree = 1, kRing = 2 };
+
+struct MeanParams {
+    RepPtrs rep;
+    float* out;
+    int64_t numel;
+    int64_t ring_base;  // ring chunk j has ring_base + (j < ring_rem) elements
+    int64_t ring_rem;
+    int32_t n;
+    int32_t pow2;       // n is a power of two: scale by the exact reciprocal
+    float inv_n;
+};
+
+// acc / n.  For n = 2^k, acc * 2^-k is the same real number as acc / 2^k, so
+// both round to the same fp32 value (subnormal results included); otherwise
+// a true IEEE division.
+__device__ __forceinline__ float scale_by_n(float acc, int32_t pow2, float inv_n, int32_t n) {
+    return pow2 ? __fmul_rn(acc, inv_n) : __fdiv_rn(acc, static_cast<float>(n));
+}
+
+// Ring chunk holding element e: N near-equal contiguous chunks, the first
+// `rem` of them one element longer.
+__device__ __forceinline__ int ring_chunk(int64_t e, int64_t base, int64_t rem) {
+    const int64_t big = rem * (base + 1);
+    return e < big ? static_cast<int>(e / (base + 1)) : static_cast<int>(rem + (e - big) / base);
+}
+
+template <bool BF16, int ORDER>
+__device__ float mean_one(const MeanParams& a, int64_t e) {
+    const int n = a.n;
+    float acc;
+    if constexpr (ORDER == kRank) {
+        acc = 0.0f;
+        for (int r = 0; r < n; ++r) acc = __fadd_rn(acc, load_elem<BF16>(a.rep.p[r], e));
+    } else if constexpr (ORDER == kTree) {
+        float t[DDP_MAX_REPLICAS];
+        for (int r = 0; r < n; ++r) t[r] = load_elem<BF16>(a.rep.p[r], e);
+        for (int w = n; w > 1; w >>= 1)
+            for (int i = 0; i < w / 2; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
+        acc = t[0];
+    } else {
+        const int j = ring_chunk(e, a.ring_base, a.ring_rem);
+        acc = load_elem<BF16>(a.rep.p[j], e);
+        for (int s = 1; s < n; ++s) {
+            int r = j + s;
+            r -= (r >= n) ? n : 0;
+            acc = __fadd_rn(acc, load_elem<BF16>(a.rep.p[r], e));
+        }
+    }
+    return scale_by_n(acc, a.pow2, a.inv_n, n);
+}
+
+template <int NMAX, bool BF16, int ORDER, bool WB, bool NC>
+__global__ void __launch_bounds__(kThreads) mean_kernel(const __grid_constant__ MeanParams a) {
+    constexpr int VEC = BF16 ? 8 : 4;   // elements per 16-byte input vector
+    constexpr int ESZ = BF16 ? 2 : 4;
+    const int n = a.n;
+    const int64_t nvec = a.numel / VEC;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+
+    for (int64_t v = gtid; v < nvec; v += stride) {
+        const int64_t e0 = v * VEC;
+        float res[VEC];
+        bool done = false;
+        uint4 raw[NMAX];
+        if constexpr (ORDER == kRing) {
+            const int j0 = ring_chunk(e0, a.ring_base, a.ring_rem);
+            const int j1 = ring_chunk(e0 + VEC - 1, a.ring_base, a.ring_rem);
+            if (j0 == j1) {
+                // load replicas rotated so that raw[s] is replica (j0 + s) mod n
+#pragma unroll
+                for (int s = 0; s < NMAX; ++s) {
+                    if (s < n) {
+                        int r = j0 + s;
+                        r -= (r >= n) ? n : 0;
+                        raw[s] = ld16<NC>(static_cast<const char*>(a.rep.p[r]) + e0 * ESZ);
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) {
+                    float acc = vec_elem<BF16>(raw[0], k);
+#pragma unroll
+                    for (int s = 1; s < NMAX; ++s)
+                        if (s < n) acc = __fadd_rn(acc, vec_elem<BF16>(raw[s], k));
+                    res[k] = scale_by_n(acc, a.pow2, a.inv_n, n);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < VEC; ++k) res[k] = mean_one<BF16, kRing>(a, e0 + k);
+            }
+            done = true;
+        }
+        if (!done) {
+#pragma unroll
+            for (int r = 0; r < NMAX; ++r)
+                if (r < n) raw[r] = ld16<NC>(static_cast<const char*>(a.rep.p[r]) + e0 * ESZ);
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                float acc;
+                if constexpr (ORDER == kRank) {
+                    acc = 0.0f;
+#pragma unroll
+                    for (int r = 0; r < NMAX; ++r)
+                        if (r < n) acc = __fadd_rn(acc, vec_elem<BF16>(raw[r], k));
+                } else {
+                    float t[NMAX];
+#pragma unroll
+                    for (int r = 0; r < NMAX; ++r) t[r] = (r < n) ? vec_elem<BF16>(raw[r], k) : 0.0f;
+#pragma unroll
+                    for (int w = NMAX; w > 1; w >>= 1)
+                        if (w <= n) {
+#pragma unroll
+                            for (int i = 0; i < w / 2; ++i) t[i] = __fadd_rn(t[2 * i], t[2 * i + 1]);
+                        }
+                    acc = t[0];
+                }
+                res[k] = scale_by_n(acc, a.pow2, a.inv_n, n);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const uint4 o = f4_bits(res[4 * q], res[4 * q + 1], res[4 * q + 2], res[4 * q + 3]);
+            st16(a.out + e0 + 4 * q, o);
+            if constexpr (WB) {
+#pragma unroll
+                for (int r = 0; r < NMAX; ++r)
+                    if (r < n && a.rep.p[r] != a.out)
+                        st16(const_cast<float*>(static_cast<const float*>(a.rep.p[r])) + e0 + 4 * q, o);
+            }
+        }
+    }
+
+    // ragged tail: the last numel % VEC elements, one per thread of block 0
+    const int64_t tail0 = nvec * VEC;
+    if (gtid < a.numel - tail0) {
+        const int64_t e = tail0 + gtid;
+        const float m = mean_one<BF16, ORDER>(a, e);
+        a.out[e] = m;
+        if constexpr (WB) {
+            for (int r = 0; r < n; ++r)
+                if (a.rep.p[r] != a.out) const_cast<float*>(static_cast<const float*>(a.rep.p[r]))[e] = m;
+        }
+    }
+}
+
+struct SgdParams {
+    RepPtrs rep;
+    float* param;
+    float* buf;
+    float* gout;
+    int64_t numel;
+    int32_t n;
+    int32_t pow2;
+    float inv_n;
+    float lr, mom, wd;
+};
+
+// d = g + wd*θ; b = μ*buf + d; θ = θ − lr*b — each operation rounded on its own.
+__device__ __forceinline__ void sgd_elem(const SgdParams& a, float g, float& th, float& b) {
+    float d = g;
+    if (a.wd != 0.0f) d = __fadd_rn(d, __fmul_rn(a.wd, th));
+    if (a.mom != 0.0f) {
+        b = __fadd_rn(__fmul_rn(a.mom, b), d);
+        d = b;
+    }
+    th = __fsub_rn(th, __fmul_rn(a.lr, d));
+}
+
+template <int NMAX, bool BF16>
+__global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ SgdParams a) {
+    constexpr int VEC = BF16 ? 8 : 4;
+    constexpr int ESZ = BF16 ? 2 : 4;
+    const int n = a.n;
+    const bool has_mom = a.mom != 0.0f;
+    const int64_t nvec = a.numel / VEC;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+
+    for (int64_t v = gtid; v < nvec; v += stride) {
+        const int64_t e0 = v * VEC;
+        uint4 raw[NMAX];
+#pragma unroll
+        for (int r = 0; r < NMAX; ++r)
+            if (r < n) raw[r] = ld16<true>(static_cast<const char*>(a.rep.p[r]) + e0 * ESZ);
+        uint4 thv[VEC / 4], bv[VEC / 4];
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            thv[q] = ld16<false>(a.param + e0 + 4 * q);
+            bv[q] = has_mom ? ld16<false>(a.buf + e0 + 4 * q) : make_uint4(0, 0, 0, 0);
+        }
+        float th[VEC], b[VEC], g[VEC];
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int r = 0; r < NMAX; ++r)
+                if (r < n) acc = __fadd_rn(acc, vec_elem<BF16>(raw[r], k));
+            g[k] = scale_by_n(acc, a.pow2, a.inv_n, n);
+            th[k] = vec_elem<false>(thv[k / 4], k % 4);
+            b[k] = vec_elem<false>(bv[k / 4], k % 4);
+            sgd_elem(a, g[k], th[k], b[k]);
+        }
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            st16(a.param + e0 + 4 * q, f4_bits(th[4 * q], th[4 * q + 1], th[4 * q + 2], th[4 * q + 3]));
+            if (has_mom) st16(a.buf + e0 + 4 * q, f4_bits(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]));
+            if (a.gout != nullptr)
+                st16(a.gout + e0 + 4 * q, f4_bits(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]));
+        }
+    }
+
+    const int64_t tail0 = nvec * VEC;
+    if (gtid < a.numel - tail0) {
+        const int64_t e = tail0 + gtid;
+        float acc = 0.0f;
+        for (int r = 0; r < n; ++r) acc = __fadd_rn(acc, load_elem<BF16>(a.rep.p[r], e));
+        const float g = scale_by_n(acc, a.pow2, a.inv_n, n);
+        float th = a.param[e];
+        float b = has_mom ? a.buf[e] : 0.0f;
+        sgd_elem(a, g, th, b);
+        a.param[e] = th;
+        if (has_mom) a.buf[e] = b;
+        if (a.gout != nullptr) a.gout[e] = g;
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+int launch_grid(int64_t nvec, int* grid) {
+    DeviceInfo d;
+    int st = current_device_info(&d);
+    if (st != DDP_OK) return st;
+    const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
+    int64_t need = (nvec + kThreads - 1) / kThreads;
+    if (need < 1) need = 1;   // block 0 also covers the ragged tail
+    *grid = static_cast<int>(need < resident ? need : resident);
+    return DDP_OK;
+}
+
+template <int NMAX, bool BF16, int ORDER, bool WB, bool NC>
+int launch_mean(const MeanParams& p, int grid, cudaStream_t s) {
+    mean_kernel<NMAX, BF16, ORDER, WB, NC><<<grid, kThreads, 0, s>>>(p);
+    return check_launch();
+}
+
+template <int NMAX, bool BF16, int ORDER>
+int dispatch_mean_mode(const MeanParams& p, int grid, cudaStream_t s, bool wb, bool aliased) {
+    if constexpr (BF16) {
+        return launch_mean<NMAX, true, ORDER, false, true>(p, grid, s);
+    } else {
+        if (wb) return launch_mean<NMAX, false, ORDER, true, false>(p, grid, s);
+        if (aliased) return launch_mean<NMAX, false, ORDER, false, false>(p, grid, s);
+        return launch_mean<NMAX, false, ORDER, false, true>(p, grid, s);
+    }
+}
+
+template <int NMAX, bool BF16>
+int dispatch_mean_order(const MeanParams& p, int grid, cudaStream_t s, int order, bool wb, bool aliased) {
+    switch (order) {
+        case kTree: return dispatch_mean_mode<NMAX, BF16, kTree>(p, grid, s, wb, aliased);
+        case kRing: return dispatch_mean_mode<NMAX, BF16, kRing>(p, grid, s, wb, aliased);
+        default: return dispatch_mean_mode<NMAX, BF16, kRank>(p, grid, s, wb, aliased);
+    }
+}
+
+template <bool BF16>
+int dispatch_mean(const MeanParams& p, int grid, cudaStream_t s, int order, bool wb, bool aliased) {
+    if (p.n <= 4) return dispatch_mean_order<4, BF16>(p, grid, s, order, wb, aliased);
+    if (p.n <= 8) return dispatch_mean_order<8, BF16>(p, grid, s, order, wb, aliased);
+    return dispatch_mean_order<16, BF16>(p, grid, s, order, wb, aliased);
+}
+
+template <bool BF16>
+int dispatch_sgd(const SgdParams& p, int grid, cudaStream_t s) {
+    if (p.n <= 4) sgd_kernel<4, BF16><<<grid, kThreads, 0, s>>>(p);
+    else if (p.n <= 8) sgd_kernel<8, BF16><<<grid, kThreads, 0, s>>>(p);
+    else sgd_kernel<16, BF16><<<grid, kThreads, 0, s>>>(p);
+    return check_launch();
+}
+
+bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+// Shared validation of the replica list.
+int check_replicas(const void* const* replicas, int32_t n, int32_t dtype, int64_t numel) {
+    if (replicas == nullptr || n < 1 || n > DDP_MAX_REPLICAS) return DDP_ERR_INVALID_ARG;
+    if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID_ARG;
+    if (numel < 0 || numel > INT64_MAX / 16) return DDP_ERR_INVALID_ARG;
+    for (int r = 0; r < n; ++r) {
+        if (replicas[r] == nullptr) return DDP_ERR_INVALID_ARG;
+        if (!aligned16(replicas[r])) return DDP_ERR_ALIGNMENT;
+    }
+    return DDP_OK;
+}
+
+}  // namespace
+}  // namespace ddp
+
+using namespace ddp;
+
+extern "C" int ddp_bucket_allreduce_mean(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                                         int64_t numel, float* out, uint32_t flags, void* stream) {
+    int st = check_replicas(replicas, n_replicas, in_dtype, numel);
+    if (st != DDP_OK) return st;
+    if (out == nullptr) return DDP_ERR_INVALID_ARG;
+    if (!aligned16(out)) return DDP_ERR_ALIGNMENT;
+    const uint32_t known = DDP_FLAG_TREE_ORDER | DDP_FLAG_WRITE_BACK_ALL | DDP_FLAG_RING_ORDER;
+    if (flags & ~known) return DDP_ERR_INVALID_ARG;
+    const bool tree = flags & DDP_FLAG_TREE_ORDER, ring = flags & DDP_FLAG_RING_ORDER;
+    const bool wb = flags & DDP_FLAG_WRITE_BACK_ALL;
+    if (tree && ring) return DDP_ERR_INVALID_ARG;
+    if (tree && !is_pow2(n_replicas)) return DDP_ERR_INVALID_ARG;
+    if (wb && in_dtype != DDP_F32) return DDP_ERR_INVALID_ARG;
+
+    const size_t esz = in_dtype == DDP_BF16 ? 2 : 4;
+    const size_t in_bytes = static_cast<size_t>(numel) * esz, out_bytes = static_cast<size_t>(numel) * 4;
+    bool aliased = false;
+    for (int r = 0; r < n_replicas; ++r) {
+        if (static_cast<const void*>(out) == replicas[r] && in_dtype == DDP_F32) {
+            aliased = true;
+        } else if (overlaps(out, out_bytes, replicas[r], in_bytes)) {
+            return DDP_ERR_INVALID_ARG;
+        }
+        if (wb)   // replicas are written: they must be disjoint or identical
+            for (int q = 0; q < r; ++q)
+                if (replicas[q] != replicas[r] && overlaps(replicas[q], in_bytes, replicas[r], in_bytes))
+                    return DDP_ERR_INVALID_ARG;
+    }
+    if (numel == 0) return DDP_OK;
+
+    MeanParams p{};
+    for (int r = 0; r < n_replicas; ++r) p.rep.p[r] = replicas[r];
+    p.out = out;
+    p.numel = numel;
+    p.n = n_replicas;
+    p.pow2 = is_pow2(n_replicas);
+    p.inv_n = 1.0f / static_cast<float>(n_replicas);   // exact when n is a power of two
+    p.ring_base = numel / n_replicas;
+    p.ring_rem = numel % n_replicas;
+    const int order = tree ? kTree : ring ? kRing : kRank;
+    const int vec = in_dtype == DDP_BF16 ? 8 : 4;
+    int grid = 0;
+    if ((st = launch_grid(numel / vec, &grid)) != DDP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return in_dtype == DDP_BF16 ? dispatch_mean<true>(p, grid, s, order, wb, aliased)
+                                : dispatch_mean<false>(p, grid, s, order, wb, aliased);
+}
+
+extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                                        int64_t numel, float* param, float* momentum_buf,
+                                        float lr, float momentum, float weight_decay,
+                                        float* grad_out, uint32_t flags, void* stream) {
+    int st = check_replicas(replicas, n_replicas, in_dtype, numel);
+    if (st != DDP_OK) return st;
+    if (flags != 0 || param == nullptr) return DDP_ERR_INVALID_ARG;
+    if (!(lr == lr) || !(momentum == momentum) || !(weight_decay == weight_decay)) return DDP_ERR_INVALID_ARG;
+    const bool has_mom = momentum != 0.0f;
+    if (has_mom != (momentum_buf != nullptr)) return DDP_ERR_INVALID_ARG;
+    if (!aligned16(param) || (momentum_buf && !aligned16(momentum_buf)) || (grad_out && !aligned16(grad_out)))
+        return DDP_ERR_ALIGNMENT;
+    const size_t esz = in_dtype == DDP_BF16 ? 2 : 4;
+    const size_t in_bytes = static_cast<size_t>(numel) * esz, fb = static_cast<size_t>(numel) * 4;
+    const void* outs[3] = {param, momentum_buf, grad_out};
+    for (int i = 0; i < 3; ++i) {
+        if (outs[i] == nullptr) continue;
+        for (int j = 0; j < i; ++j)
+            if (outs[j] != nullptr && overlaps(outs[i], fb, outs[j], fb)) return DDP_ERR_INVALID_ARG;
+        for (int r = 0; r < n_replicas; ++r)
+            if (overlaps(outs[i], fb, replicas[r], in_bytes)) return DDP_ERR_INVALID_ARG;
+    }
+    if (numel == 0) return DDP_OK;
+
+    SgdParams p{};
+    for (int r = 0; r < n_replicas; ++r) p.rep.p[r] = replicas[r];
+    p.param = param;
+    p.buf = momentum_buf;
+    p.gout = grad_out;
+    p.numel = numel;
+    p.n = n_replicas;
+    p.pow2 = is_pow2(n_replicas);
+    p.inv_n = 1.0f / static_cast<float>(n_replicas);
+    p.lr = lr;
+    p.mom = momentum;
+    p.wd = weight_decay;
+    int grid = 0;
+    if ((st = launch_grid(numel / (in_dtype == DDP_BF16 ? 8 : 4), &grid)) != DDP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return in_dtype == DDP_BF16 ? dispatch_sgd<true>(p, grid, s) : dispatch_sgd<false>(p, grid, s);
+}

@@ -1,0 +1,92 @@
+// Device helpers shared by the library's kernels: 16-byte global accesses
+// with explicit cache policy, and the exact bf16 -> fp32 widening.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace ddp {
+
+constexpr int kThreads = 256;
+
+// 16-byte global load.  NC = true: read-only (non-coherent) path without L1
+// allocation, for buffers the kernel never writes; every element is read
+// exactly once, so nothing is worth caching.  NC = false: coherent streaming
+// load, for buffers the same kernel also writes (in-place updates).
+template <bool NC>
+__device__ __forceinline__ uint4 ld16(const void* p) {
+    uint4 v;
+    if constexpr (NC) {
+        asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+            : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+            : "l"(p));
+    } else {
+        asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                     : "l"(p)
+                     : "memory");
+    }
+    return v;
+}
+
+// 16-byte streaming store (evict-first: the result is not re-read by this kernel).
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 f4_bits(float a, float b, float c, float d) {
+    return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
+}
+
+// bf16 -> fp32 is exact: the bf16 pattern is the high half of the fp32 pattern.
+// A 32-bit word holds two bf16 values, element 0 in the low half.
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Element k of a 16-byte vector holding 4 fp32 or 8 bf16 values, as fp32.
+template <bool BF16>
+__device__ __forceinline__ float vec_elem(const uint4& v, int k) {
+    const uint32_t w = (k >> (BF16 ? 1 : 0)) == 0 ? v.x : (k >> (BF16 ? 1 : 0)) == 1 ? v.y
+                     : (k >> (BF16 ? 1 : 0)) == 2 ? v.z : v.w;
+    if constexpr (BF16) return (k & 1) ? bf16_hi(w) : bf16_lo(w);
+    else return __uint_as_float(w);
+}
+
+// One element of a flat fp32 or bf16 buffer, as fp32 (scalar path).
+template <bool BF16>
+__device__ __forceinline__ float load_elem(const void* base, int64_t e) {
+    if constexpr (BF16) {
+        const unsigned short h = reinterpret_cast<const unsigned short*>(base)[e];
+        return __uint_as_float(static_cast<uint32_t>(h) << 16);
+    } else {
+        return reinterpret_cast<const float*>(base)[e];
+    }
+}
+
+}  // namespace ddp
+
+namespace ddp {
+
+// Division of unsigned 32-bit values n < 2^31 by a fixed divisor 1 <= d < 2^31
+// with one multiply-high, add and shift (Granlund & Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, round-up variant):
+// s = ceil(log2 d), m = floor(2^32 (2^s - d) / d) + 1, q = (mulhi(n, m) + n) >> s.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f{d, 0, 0};
+    while ((uint64_t(1) << f.s) < d) ++f.s;
+    f.m = static_cast<uint32_t>(((uint64_t(1) << 32) * ((uint64_t(1) << f.s) - d)) / d + 1);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+    return (__umulhi(n, f.m) + n) >> f.s;
+}
+
+}  // namespace ddp

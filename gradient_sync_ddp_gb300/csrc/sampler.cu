@@ -1,0 +1,162 @@
+// DistributedSampler index lists, one thread per output index.
+//
+// AI_Infra notes "1.DataParallel / DDP" §4.4: num_samples = ceil(n/N) (or
+// floor with drop_last), total = num_samples*N; the list 0..n-1 is shuffled
+// with a generator seeded by seed+epoch (the same on every rank, so no
+// communication is needed), padded by repeating its head up to total (or cut
+// to total), and rank r takes positions r, r+N, r+2N, ...
+//
+// The shuffle is a keyed permutation that any thread evaluates for any
+// position on its own: a 4-round balanced Feistel network on 2h bits
+// (h = ceil(ceil(log2 n)/2)), round keys = the first four SplitMix64 outputs
+// from state seed+epoch, round function = the SplitMix64 output mix (Steele,
+// Lea & Flood, OOPSLA 2014) truncated to h bits, and cycle walking (encrypt
+// again while the value is >= n).  Each walk is bounded: after 4096
+// encryptions the thread writes -1 and counts the index in a status word
+// instead of looping on.  The kernel is integer-ALU bound (~4 rounds x
+// ~3.3 walks x 2 64-bit multiplies per index); the 8-byte output per index
+// is its only memory traffic.
+#include <cstdint>
+
+#include "common.cuh"
+#include "host_common.h"
+
+namespace ddp {
+namespace {
+
+constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
+constexpr int kRounds = 4;
+constexpr int kWalkCap = 4096;
+
+struct SamplerParams {
+    int64_t* out;
+    int32_t* status;
+    uint64_t rk[kRounds];
+    uint64_t n;          // items
+    uint64_t mask;       // 2^h - 1
+    int64_t ns;          // num_samples
+    int64_t count;       // outputs to write
+    int32_t N;           // replicas
+    int32_t rank;        // -1: all ranks, rank-major
+    int32_t h;
+    int32_t shuffle;
+};
+
+__host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ uint64_t encrypt(uint64_t x, const SamplerParams& a) {
+    uint64_t L = x >> a.h, R = x & a.mask;
+#pragma unroll
+    for (int i = 0; i < kRounds; ++i) {
+        const uint64_t F = mix64(R ^ a.rk[i]) & a.mask;
+        const uint64_t t = L ^ F;
+        L = R;
+        R = t;
+    }
+    return (L << a.h) | R;
+}
+
+__global__ void __launch_bounds__(kThreads) sampler_kernel(const __grid_constant__ SamplerParams a) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < a.count; i += stride) {
+        int64_t r, s;
+        if (a.rank >= 0) {
+            r = a.rank;
+            s = i;
+        } else {
+            r = i / a.ns;
+            s = i - r * a.ns;
+        }
+        const uint64_t pos = static_cast<uint64_t>(r) + static_cast<uint64_t>(s) * static_cast<uint64_t>(a.N);
+        const uint64_t j = pos < a.n ? pos : pos % a.n;       // padding repeats the head
+        int64_t v = static_cast<int64_t>(j);
+        if (a.shuffle && a.n > 1) {
+            uint64_t y = encrypt(j, a);
+            int steps = 1;
+            while (y >= a.n) {
+                if (steps >= kWalkCap) break;
+                y = encrypt(y, a);
+                ++steps;
+            }
+            if (y >= a.n) {
+                v = -1;
+                if (a.status) atomicAdd(a.status, 1);
+            } else {
+                v = static_cast<int64_t>(y);
+            }
+        }
+        a.out[i] = v;
+    }
+}
+
+}  // namespace
+}  // namespace ddp
+
+using namespace ddp;
+
+extern "C" int64_t dist_sampler_num_samples(int64_t n_items, int32_t n_replicas, int32_t drop_last) {
+    if (n_items < 0 || n_items >= (int64_t(1) << 62) || n_replicas < 1 || (drop_last != 0 && drop_last != 1))
+        return -1;
+    return drop_last ? n_items / n_replicas : (n_items + n_replicas - 1) / n_replicas;
+}
+
+extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t rank,
+                                    uint64_t seed, uint64_t epoch, int32_t shuffle, int32_t drop_last,
+                                    int64_t* out, int64_t out_capacity, int64_t* num_samples_out,
+                                    int32_t* walk_status, void* stream) {
+    if (num_samples_out == nullptr) return DDP_ERR_INVALID_ARG;
+    if (shuffle != 0 && shuffle != 1) return DDP_ERR_INVALID_ARG;
+    const int64_t ns = dist_sampler_num_samples(n_items, n_replicas, drop_last);
+    if (ns < 0 || rank < -1 || rank >= n_replicas || out_capacity < 0) return DDP_ERR_INVALID_ARG;
+    *num_samples_out = ns;
+    const int64_t count = rank >= 0 ? ns : ns * n_replicas;
+    if (out_capacity < count) return DDP_ERR_CAPACITY;
+    if (count > 0 && out == nullptr) return DDP_ERR_INVALID_ARG;
+    if (out != nullptr && (reinterpret_cast<uintptr_t>(out) & 7u)) return DDP_ERR_ALIGNMENT;
+    if (walk_status != nullptr && (reinterpret_cast<uintptr_t>(walk_status) & 3u)) return DDP_ERR_ALIGNMENT;
+    if (walk_status != nullptr && overlaps(walk_status, 4, out, static_cast<size_t>(count) * 8))
+        return DDP_ERR_INVALID_ARG;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (walk_status != nullptr) {
+        cudaError_t e = cudaMemsetAsync(walk_status, 0, sizeof(int32_t), s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (count == 0) return DDP_OK;
+
+    SamplerParams p{};
+    p.out = out;
+    p.status = walk_status;
+    const uint64_t key = seed + epoch;            // mod 2^64
+    uint64_t state = key;
+    for (int i = 0; i < kRounds; ++i) {           // SplitMix64 stream from `key`
+        state += kGamma;
+        p.rk[i] = mix64(state);
+    }
+    const uint64_t n = static_cast<uint64_t>(n_items);
+    int bits = 1;
+    while (bits < 63 && (uint64_t(1) << bits) < n) ++bits;   // smallest bits >= 1 with 2^bits >= n
+    p.h = (bits + 1) / 2;
+    p.mask = (uint64_t(1) << p.h) - 1;
+    p.n = n;
+    p.ns = ns;
+    p.count = count;
+    p.N = n_replicas;
+    p.rank = rank;
+    p.shuffle = shuffle;
+
+    DeviceInfo d;
+    int st = current_device_info(&d);
+    if (st != DDP_OK) return st;
+    const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
+    int64_t grid = (count + kThreads - 1) / kThreads;
+    if (grid > resident) grid = resident;
+    sampler_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    return check_launch();
+}

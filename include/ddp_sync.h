@@ -1,0 +1,268 @@
+/*
+ * ddp_sync.h — C ABI of the GB300 (sm_103a) DDP gradient-synchronisation library
+ * (libddp_sync.so).
+ *
+ * The library implements, on one GPU, the data-parallel hot path of DDP
+ * training: N model replicas' gradients are N resident device buffers, and the
+ * library averages them bucket by bucket (optionally fused with the bf16 ->
+ * fp32 widen and an SGD step), merges SyncBatchNorm statistics across the
+ * replicas and applies the normalisation, and produces DistributedSampler
+ * index lists.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [TR24] Tech-Renaissance, "(24) NCCL通信与分布式数据并行"
+ *   [TR16] Tech-Renaissance, "(16) DTensor"
+ *   [DDP]  AI_Infra notes, "1.DataParallel / DDP"
+ *
+ * Conventions shared by every entry point
+ *   - Plain C types only.  Device pointers are CUDA device addresses on the
+ *     current device; host pointers are ordinary host memory.  `stream` is a
+ *     cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Ownership: the caller owns every buffer.  No entry point allocates or
+ *     frees memory, synchronises the device, or keeps a pointer after it
+ *     returns.  Host arrays (e.g. the list of replica pointers) are read
+ *     during the call only; their contents are copied into the kernel's
+ *     launch parameters, so the calls may be captured into a CUDA Graph.
+ *   - Asynchrony: work is enqueued on `stream` and the call returns at once.
+ *     Results are valid once the stream has reached that point.
+ *   - Errors: every entry point returns an int status (ddp_status below) and
+ *     never throws or aborts.  Arguments are validated on the host before any
+ *     CUDA call; an invalid call enqueues nothing and leaves every buffer
+ *     untouched.  A failed kernel launch returns DDP_ERR_CUDA and the CUDA
+ *     error code is available from ddp_last_cuda_error() on the same thread.
+ *   - Alignment: every device pointer must be 16-byte aligned
+ *     (DDP_ERR_ALIGNMENT otherwise); bucket offsets from ddp_plan_buckets are
+ *     256-byte aligned, so pointers into planned buffers always qualify.
+ *   - Replica count: 1 <= n_replicas <= DDP_MAX_REPLICAS.
+ *   - Arithmetic: no fused multiply-add in the bit-exact paths, IEEE
+ *     round-to-nearest-even on every fp32 operation, subnormals preserved.
+ */
+#ifndef DDP_SYNC_H
+#define DDP_SYNC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DDP_MAX_REPLICAS 16
+
+typedef enum {
+    DDP_OK = 0,
+    DDP_ERR_INVALID_ARG = -1,   /* null pointer, negative size, bad enum, bad overlap */
+    DDP_ERR_ALIGNMENT = -2,     /* a device pointer is not 16-byte aligned */
+    DDP_ERR_CAPACITY = -3,      /* an output array or workspace is too small */
+    DDP_ERR_CUDA = -4,          /* a CUDA call failed; see ddp_last_cuda_error() */
+    DDP_ERR_UNSUPPORTED = -5,   /* valid request this build does not implement */
+    DDP_ERR_TIMEOUT = -6        /* a bounded wait or loop ran out (see each entry) */
+} ddp_status;
+
+typedef enum { DDP_F32 = 0, DDP_BF16 = 1 } ddp_dtype;
+
+/* bucket planning modes */
+enum { DDP_PLAN_CAP = 0, DDP_PLAN_DEEP_FIRST = 1 };
+
+/* summation-order / output flags of the all-reduce entry points */
+enum {
+    DDP_FLAG_TREE_ORDER = 1u,      /* pairwise tree order (power-of-two N) */
+    DDP_FLAG_WRITE_BACK_ALL = 2u,  /* also store the result into every replica (fp32 only) */
+    DDP_FLAG_RING_ORDER = 4u       /* chunk-rotated order of a ring all-reduce */
+};
+
+/* One bucket of a plan: a contiguous range of the flat gradient buffer. */
+typedef struct {
+    int64_t offset_elems;   /* first element of the bucket in the flat buffer */
+    int64_t numel;          /* elements in the bucket (tensors packed back to back) */
+    int32_t first;          /* index into `order` of the bucket's first tensor */
+    int32_t count;          /* number of tensors in the bucket */
+} ddp_bucket;
+
+/*
+ * ddp_plan_buckets — partition a model's gradient tensors into flat buckets.
+ *
+ * [DDP] §3.2 and §4.2: buckets are built over the parameters in reverse
+ * registration order (the last layer's gradient is ready first) with a size
+ * cap (25 MB by default).  [TR24] §八: the two-bucket split, DEEP first,
+ * then FIRST.  [TR16] §四/§六: one flat buffer, bucket bases aligned.
+ *
+ *   n_tensors       number of tensors T (>= 0)
+ *   numels          host int64[T], element count of each tensor in
+ *                   registration order (each >= 0)
+ *   elem_bytes      bytes per gradient element (2 or 4)
+ *   cap_bytes       DDP_PLAN_CAP: close a bucket before a tensor whose bytes
+ *                   would push it past cap_bytes (a tensor larger than the
+ *                   cap is alone); ignored for DDP_PLAN_DEEP_FIRST.  >= 0.
+ *   mode            DDP_PLAN_CAP or DDP_PLAN_DEEP_FIRST
+ *   is_first        host uint8[T] (DDP_PLAN_DEEP_FIRST only, else may be
+ *                   NULL): nonzero puts the tensor in the FIRST bucket.
+ *   align_bytes     bucket base alignment in bytes: a positive multiple of
+ *                   elem_bytes and of 16 (256 = [TR16] align_up_256)
+ *   buckets         host ddp_bucket[max_buckets], written [0, *n_buckets)
+ *   n_buckets       host int32*, receives the number of buckets
+ *   order           host int32[T]: tensor ids in flat-buffer order
+ *   tensor_offset   host int64[T]: element offset of each tensor id
+ *   tensor_bucket   host int32[T]: bucket of each tensor id
+ *   total_elems     host int64*: flat buffer length, end of the last bucket
+ *                   rounded up to the alignment
+ * Host-only; no CUDA call.  Returns DDP_ERR_CAPACITY (with *n_buckets set to
+ * the number needed) if max_buckets is too small.
+ */
+int ddp_plan_buckets(int32_t n_tensors, const int64_t* numels, int32_t elem_bytes, int64_t cap_bytes,
+                     int32_t mode, const uint8_t* is_first, int32_t align_bytes,
+                     ddp_bucket* buckets, int32_t max_buckets, int32_t* n_buckets,
+                     int32_t* order, int64_t* tensor_offset, int32_t* tensor_bucket,
+                     int64_t* total_elems);
+
+/*
+ * ddp_bucket_allreduce_mean — average one bucket over N replicas.
+ *
+ * [TR24] §一: grad_sync = 0; for r in 0..N-1: grad_sync += grad[r];
+ * grad_sync /= float(N).  [TR24] §九 / [DDP] §4.2: sum all-reduce then
+ * scale by 1/world_size, fused here into one pass.  [TR24] §十一: an AMP
+ * gradient cast precedes the all-reduce; bf16 replicas are widened to fp32
+ * exactly inside the same pass.
+ *
+ *   replicas    host array of n_replicas device pointers, replica r's bucket
+ *               (numel elements of in_dtype, 16-byte aligned)
+ *   n_replicas  N, 1..DDP_MAX_REPLICAS
+ *   in_dtype    DDP_F32 or DDP_BF16
+ *   numel       elements in the bucket (>= 0; 0 enqueues nothing)
+ *   out         device float[numel], 16-byte aligned: the fp32 average.  It
+ *               may be exactly equal to a replica pointer when in_dtype is
+ *               DDP_F32 (in place, like ncclAllReduce); any other overlap
+ *               with a replica is rejected.
+ *   flags       0 = rank order (bit-exact with the definition above; the
+ *               1/N scale is a multiply by the exact reciprocal when N is a
+ *               power of two and a true division otherwise — identical
+ *               results); DDP_FLAG_TREE_ORDER = ((g0+g1)+(g2+g3))+... then
+ *               /N (N a power of two); DDP_FLAG_RING_ORDER = element e of
+ *               chunk j (N near-equal contiguous chunks, longer ones first)
+ *               is summed g_j, g_j+1, ..., g_j-1 (mod N) then /N, the order
+ *               of the ring all-reduce of [DDP] §2.11; DDP_FLAG_WRITE_BACK_ALL
+ *               (DDP_F32 only) also stores the average into every replica.
+ *               TREE and RING are exclusive.
+ *   stream      cudaStream_t as void*
+ */
+int ddp_bucket_allreduce_mean(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                              int64_t numel, float* out, uint32_t flags, void* stream);
+
+/*
+ * ddp_bucket_allreduce_sgd — average one bucket and apply the SGD step.
+ *
+ * [DDP] §5.3: θ ← θ − η·g with g the synced average; [DDP] §3.1: every rank
+ * applies the same deterministic step.  [TR24] §九 (note) suggests folding
+ * the 1/world_size into the optimizer kernel; this entry does that.
+ * Momentum and weight decay follow PyTorch's SGD (dampening 0, no
+ * Nesterov), each fp32 operation rounded separately:
+ *     g = mean (as ddp_bucket_allreduce_mean, rank order)
+ *     d = g + weight_decay*θ                 (if weight_decay != 0)
+ *     b = momentum*buf + d; buf = b; d = b   (if momentum != 0)
+ *     θ = θ − lr*d
+ *
+ *   replicas, n_replicas, in_dtype, numel   as for the mean
+ *   param         device float[numel], θ, updated in place
+ *   momentum_buf  device float[numel], updated in place; required iff
+ *                 momentum != 0 (else must be NULL).  Start it at zero.
+ *   lr, momentum, weight_decay   finite fp32 scalars
+ *   grad_out      device float[numel] or NULL: also store g
+ *   flags         0 (reserved)
+ * param, momentum_buf and grad_out must not overlap each other or any
+ * replica.
+ */
+int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                             int64_t numel, float* param, float* momentum_buf,
+                             float lr, float momentum, float weight_decay,
+                             float* grad_out, uint32_t flags, void* stream);
+
+/*
+ * syncbn_workspace_bytes — device workspace that syncbn_merge_apply needs
+ * for these sizes (0 for invalid sizes).
+ */
+size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int32_t H, int32_t W);
+
+/*
+ * syncbn_merge_apply — strict SyncBatchNorm forward across N replicas.
+ *
+ * [TR24] §十二: strict SyncBatchNorm all-reduces each rank's per-channel sum
+ * and sum of squares before BN finalize/apply.  [DDP] §4.3: the statistics
+ * are those of the global batch.  Per channel c:
+ *     S = Σ_r Σ x_r[:,c],  Q = Σ_r Σ x_r[:,c]²,  M = N·batch·H·W
+ *     mean = S/M,  var = Q/M − mean²  (biased),  invstd = 1/sqrt(var + eps)
+ *     y_r = (x_r − mean)·invstd·γ + β
+ * Partial sums are fp32 over at most a few hundred elements, combined and
+ * merged in fp64; the apply runs in fp32.
+ *
+ *   x            host array of n_replicas device pointers, each
+ *                [batch, C, H, W] NCHW contiguous, in_dtype elements
+ *   in_dtype     DDP_BF16 or DDP_F32
+ *   batch,C,H,W  local batch and shape, each >= 1
+ *   eps          > 0
+ *   gamma, beta  device float[C] or NULL (γ = 1, β = 0)
+ *   y            host array of n_replicas device pointers, same shape,
+ *                out_dtype elements; y[r] may equal x[r] when the dtypes
+ *                match (in place), no other overlap
+ *   mean_out, invstd_out   device float[C] each
+ *   workspace    device buffer of >= syncbn_workspace_bytes(...) bytes,
+ *                16-byte aligned, contents ignored on entry
+ */
+int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtype,
+                       int32_t batch, int32_t C, int32_t H, int32_t W, float eps,
+                       const float* gamma, const float* beta,
+                       void* const* y, int32_t out_dtype, float* mean_out, float* invstd_out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * dist_sampler_num_samples — indices per rank ([DDP] §4.4):
+ * floor(n/N) with drop_last, else ceil(n/N).  -1 on invalid input.
+ */
+int64_t dist_sampler_num_samples(int64_t n_items, int32_t n_replicas, int32_t drop_last);
+
+/*
+ * dist_sampler_indices — DistributedSampler index lists.
+ *
+ * [DDP] §4.4: num_samples = drop_last ? n/N : ceil(n/N); total =
+ * num_samples·N; the (shuffled) list 0..n-1 is padded by repeating its head
+ * up to total (or cut to total with drop_last); rank r takes positions
+ * r, r+N, r+2N, ...  The shuffle is a permutation keyed by seed+epoch so
+ * every rank agrees without communication: a 4-round balanced Feistel
+ * network on 2·ceil(ceil(log2 n)/2) bits whose round keys are the first four
+ * SplitMix64 outputs from state seed+epoch and whose round function is the
+ * SplitMix64 output mix, with cycle walking into [0, n).
+ *
+ *   n_items        n >= 0 (< 2^62)
+ *   n_replicas     N >= 1
+ *   rank           0..N-1 for one rank's list, or -1 for all ranks,
+ *                  rank-major [N][num_samples]
+ *   seed, epoch    the permutation key is seed + epoch (mod 2^64)
+ *   shuffle, drop_last   0 or 1
+ *   out            device int64[out_capacity]
+ *   out_capacity   elements available at out; must be >= num_samples
+ *                  (rank >= 0) or N·num_samples (rank == -1), else
+ *                  DDP_ERR_CAPACITY with *num_samples_out still set
+ *   num_samples_out  host int64*, receives num_samples (computed on the host)
+ *   walk_status    device int32 or NULL: set to 0, then to the number of
+ *                  indices whose cycle walk exceeded 4096 encryptions (those
+ *                  outputs are -1).  Never observed; the bound keeps every
+ *                  thread's loop finite.
+ */
+int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t rank,
+                         uint64_t seed, uint64_t epoch, int32_t shuffle, int32_t drop_last,
+                         int64_t* out, int64_t out_capacity, int64_t* num_samples_out,
+                         int32_t* walk_status, void* stream);
+
+/* Human-readable name of a ddp_status value (static string). */
+const char* ddp_status_string(int status);
+
+/* CUDA error code (cudaError_t as int) of the last DDP_ERR_CUDA on this thread. */
+int ddp_last_cuda_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* ddp_sync_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDP_SYNC_H */
