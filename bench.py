@@ -274,8 +274,8 @@ def run_ours(args, world, rank, local):
     import torch.distributed as dist
 
     import workloads
-    from gradient_sync_ddp_gb300 import build as _b
-    _b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import gradient_sync_ddp_gb300 as g
 
     if not torch.cuda.is_available():

@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libddp_sync.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libddp_sync.so is not built ({LIB_PATH}); run "
-                      "`python -m gradient_sync_ddp_gb300.build` (needs nvcc)")
+                      "`python gradient_sync_ddp_gb300/build.py` or `__graft_entry__.build()` (needs nvcc)")
 
 _lib = ctypes.CDLL(LIB_PATH)
 

@@ -6,7 +6,8 @@ device code is compiled for exactly one target, ``sm_103a``, without fast-math
 (subnormals kept, IEEE division and square root, no flush-to-zero); the host
 code with ``-ffp-contract=off``.
 
-Usage: ``python -m gradient_sync_ddp_gb300.build [--force] [--verbose]``.
+Usage: ``python gradient_sync_ddp_gb300/build.py [--force] [--verbose] [--ptxas]``
+(run it by path: importing the package needs the library this builds).
 """
 from __future__ import annotations
 

@@ -317,7 +317,7 @@ int check_replicas(const void* const* replicas, int32_t n, int32_t dtype, int64_
     if (dtype != DDP_F32 && dtype != DDP_BF16) return DDP_ERR_INVALID_ARG;
     if (numel < 0 || numel > INT64_MAX / 16) return DDP_ERR_INVALID_ARG;
     for (int r = 0; r < n; ++r) {
-        if (replicas[r] == nullptr) return DDP_ERR_INVALID_ARG;
+        if (replicas[r] == nullptr && numel > 0) return DDP_ERR_INVALID_ARG;
         if (!aligned16(replicas[r])) return DDP_ERR_ALIGNMENT;
     }
     return DDP_OK;
@@ -332,7 +332,7 @@ extern "C" int ddp_bucket_allreduce_mean(const void* const* replicas, int32_t n_
                                          int64_t numel, float* out, uint32_t flags, void* stream) {
     int st = check_replicas(replicas, n_replicas, in_dtype, numel);
     if (st != DDP_OK) return st;
-    if (out == nullptr) return DDP_ERR_INVALID_ARG;
+    if (out == nullptr && numel > 0) return DDP_ERR_INVALID_ARG;
     if (!aligned16(out)) return DDP_ERR_ALIGNMENT;
     const uint32_t known = DDP_FLAG_TREE_ORDER | DDP_FLAG_WRITE_BACK_ALL | DDP_FLAG_RING_ORDER;
     if (flags & ~known) return DDP_ERR_INVALID_ARG;
@@ -382,10 +382,11 @@ extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_r
                                         float* grad_out, uint32_t flags, void* stream) {
     int st = check_replicas(replicas, n_replicas, in_dtype, numel);
     if (st != DDP_OK) return st;
-    if (flags != 0 || param == nullptr) return DDP_ERR_INVALID_ARG;
+    if (flags != 0 || (param == nullptr && numel > 0)) return DDP_ERR_INVALID_ARG;
     if (!(lr == lr) || !(momentum == momentum) || !(weight_decay == weight_decay)) return DDP_ERR_INVALID_ARG;
     const bool has_mom = momentum != 0.0f;
-    if (has_mom != (momentum_buf != nullptr)) return DDP_ERR_INVALID_ARG;
+    if (has_mom && momentum_buf == nullptr && numel > 0) return DDP_ERR_INVALID_ARG;
+    if (!has_mom && momentum_buf != nullptr) return DDP_ERR_INVALID_ARG;
     if (!aligned16(param) || (momentum_buf && !aligned16(momentum_buf)) || (grad_out && !aligned16(grad_out)))
         return DDP_ERR_ALIGNMENT;
     const size_t esz = in_dtype == DDP_BF16 ? 2 : 4;

@@ -10,12 +10,16 @@
 //   1. stats  — grid (C, S): CTA (c, s) reduces slice s of the N*batch planes
 //      of channel c (each plane is H*W contiguous elements of one replica and
 //      one sample).  Threads stream 16-byte vectors when a plane's length is
-//      a multiple of the vector width, single elements otherwise; each vector
-//      is summed pairwise in fp32 (squares of bf16 values are exact in fp32),
-//      a thread accumulates at most a few hundred elements in fp32, and the
-//      CTA combines its threads in fp64 into workspace partials.
+//      a multiple of the vector width, single elements otherwise.  The sums
+//      are shifted by K_c, the channel's first element (replica 0, sample 0):
+//      d = x − K_c, and Σd, Σd² are accumulated, so Q/M − mean² never
+//      subtracts two large nearly equal numbers when |mean| >> std.  Each
+//      vector is summed pairwise in fp32, a thread accumulates at most a few
+//      hundred elements in fp32, and the CTA combines its threads in fp64
+//      into workspace partials.
 //   2. merge  — one thread per channel sums the S partials in fixed order in
-//      fp64: mean = S/M, var = Q/M − mean², invstd = 1/sqrt(var + eps); it
+//      fp64: with m' = Σd/M, mean = K_c + m', var = Σd²/M − m'² (the same
+//      S/M and Q/M − mean² up to rounding), invstd = 1/sqrt(var + eps); it
 //      stores per channel (m_hi, m_lo, scale, β) where m_hi + m_lo is the
 //      mean as an fp32 pair and scale = invstd·γ.
 //   3. apply  — y = ((x − m_hi) − m_lo)·scale + β over every replica, 16-byte
@@ -84,6 +88,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constan
     const uint32_t units = static_cast<uint32_t>(a.HW / W);     // accesses per plane
     const uint32_t total = static_cast<uint32_t>(p1 - p0) * units;
 
+    const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
     float acc_s = 0.0f, acc_q = 0.0f;
     for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
         const uint32_t pl_off = fdiv(t, a.div_unit);
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constan
             float e[W], q[W];
 #pragma unroll
             for (int k = 0; k < W; ++k) {
-                e[k] = vec_elem<BF16>(raw, k);
+                e[k] = __fsub_rn(vec_elem<BF16>(raw, k), K);
                 q[k] = e[k] * e[k];
             }
 #pragma unroll
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constan
             acc_s += e[0];
             acc_q += q[0];
         } else {
-            const float v = load_elem<BF16>(p, 0);
+            const float v = __fsub_rn(load_elem<BF16>(p, 0), K);
             acc_s += v;
             acc_q += v * v;
         }
@@ -121,6 +126,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constan
     if (threadIdx.x == 0) a.partial[static_cast<int64_t>(c) * a.S + s] = make_double2(ds, dq);
 }
 
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads) bn_merge_kernel(const __grid_constant__ BnParams a) {
     const int c = blockIdx.x * kThreads + threadIdx.x;
     if (c >= a.C) return;
@@ -131,8 +137,10 @@ __global__ void __launch_bounds__(kThreads) bn_merge_kernel(const __grid_constan
         Q += v.y;
     }
     const double M = static_cast<double>(a.n) * a.batch * a.HW;
-    const double mean = S / M;
-    const double var = Q / M - mean * mean;
+    const double K = static_cast<double>(load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW));
+    const double ms = S / M;
+    const double mean = K + ms;
+    const double var = Q / M - ms * ms;
     const double invstd = 1.0 / sqrt(var + static_cast<double>(a.eps));
     const double g = a.gamma ? static_cast<double>(a.gamma[c]) : 1.0;
     const double b = a.beta ? static_cast<double>(a.beta[c]) : 0.0;
@@ -335,7 +343,8 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     }
     int st = check_launch();
     if (st != DDP_OK) return st;
-    bn_merge_kernel<<<(C + kThreads - 1) / kThreads, kThreads, 0, s>>>(p);
+    if (bf16_in) bn_merge_kernel<true><<<(C + kThreads - 1) / kThreads, kThreads, 0, s>>>(p);
+    else bn_merge_kernel<false><<<(C + kThreads - 1) / kThreads, kThreads, 0, s>>>(p);
     if ((st = check_launch()) != DDP_OK) return st;
 
     DeviceInfo d;

@@ -34,6 +34,8 @@
  *     (DDP_ERR_ALIGNMENT otherwise); bucket offsets from ddp_plan_buckets are
  *     256-byte aligned, so pointers into planned buffers always qualify.
  *   - Replica count: 1 <= n_replicas <= DDP_MAX_REPLICAS.
+ *   - Empty requests: with numel == 0 (or an empty sampler list) nothing is
+ *     enqueued and the data pointers may be NULL.
  *   - Arithmetic: no fused multiply-add in the bit-exact paths, IEEE
  *     round-to-nearest-even on every fp32 operation, subnormals preserved.
  */

@@ -8,8 +8,8 @@ def load_library():
     """Build (if stale) and import the package; fails loudly without CUDA."""
     if not torch.cuda.is_available():
         raise RuntimeError("GPU tests need CUDA")
-    from gradient_sync_ddp_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import gradient_sync_ddp_gb300 as pkg
     return pkg
 

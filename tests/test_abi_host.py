@@ -17,8 +17,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def g():
-    from gradient_sync_ddp_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import gradient_sync_ddp_gb300 as pkg
     return pkg
 

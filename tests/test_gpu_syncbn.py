@@ -4,7 +4,9 @@ Tolerances (the computation is not bit-reproducible by design: fp32 partial
 sums, fp64 merge, fp32 apply):
   mean, invstd       |gpu − oracle| <= 1e-5 · |oracle| (+1e-7 absolute for a mean near 0)
   y (fp32 output)    |gpu − oracle| <= 1e-5 · |oracle| + 1e-6
-  y (bf16 output)    within one bf16 ulp of the oracle's fp64 value rounded to bf16
+  y (bf16 output)    within one bf16 ulp of the oracle's fp64 value rounded to
+                     bf16, plus the fp32 allowance above (the fp32 result
+                     may sit on the other side of a bf16 rounding boundary)
 """
 import numpy as np
 import pytest
@@ -36,13 +38,21 @@ def _check_stats(mean, invstd, m_w, s_w, what):
 
 
 def _check_y(y_t, y_w, what):
+    y_w = np.asarray(y_w, np.float64)
     if y_t.dtype == torch.bfloat16:
         got = y_t.float().cpu().numpy().astype(np.float64)
         want = oracle.f64_to_bf16_rne(y_w)
-        assert np.all(np.abs(got - want) <= _bf16_ulp(want) * 1.0001), what
+        tol = _bf16_ulp(want) * 1.0001 + 1e-5 * np.abs(y_w) + 1e-6
     else:
         got = y_t.cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(got - y_w) <= 1e-5 * np.abs(y_w) + 1e-6), what
+        want = y_w
+        tol = 1e-5 * np.abs(y_w) + 1e-6
+    err = np.abs(got - want)
+    if not np.all(err <= tol):
+        i = int(np.argmax(err - tol))
+        raise AssertionError(f"{what}: {int((err > tol).sum())} of {err.size} outside tolerance; worst at flat "
+                             f"{i}: gpu {got.reshape(-1)[i]!r} oracle {want.reshape(-1)[i]!r} "
+                             f"(fp64 {y_w.reshape(-1)[i]!r}) tol {tol.reshape(-1)[i]!r}")
 
 
 def _run(g, xs_dev, ys_dev, C, eps=1e-5, gamma=None, beta=None):
@@ -133,3 +143,20 @@ def test_full_size_shapes_sampled(g, C, H, W):
             y_w = (xv - m_w) * s_w
             got = ys[r][:, c].reshape(B, H * W)[torch.from_numpy(b).cuda(), torch.from_numpy(hw).cuda()]
             _check_y(got, y_w, f"C={C} c={c} r={r}")
+
+
+def test_large_mean_small_std(g):
+    """|mean| >> std: fp32 activations N(1000, 0.1).  Q/M − mean² would
+    cancel 8 decimal digits; the shifted sums keep invstd within tolerance."""
+    n, B, C, H, W = 4, 8, 3, 16, 16
+    gen = np.random.Generator(np.random.PCG64(1000))
+    xs = [(gen.standard_normal((B, C, H, W)) * 0.1 + 1000.0).astype(np.float32) for _ in range(n)]
+    ys = [torch.empty((B, C, H, W), device="cuda") for _ in range(n)]
+    mean, invstd = _run(g, [dev_f32(x) for x in xs], ys, C)
+    m_w, s_w, y_w = oracle.syncbn(xs, 1e-5, dtype="f32")
+    _check_stats(mean, invstd, m_w, s_w, "large mean")
+    for r in range(n):
+        got = ys[r].cpu().numpy().astype(np.float64)
+        # x − mean is exact in fp32 near 1000 only to ~6e-5 absolute (fp32 spacing of the input
+        # itself): y inherits that times invstd ≈ 10, so compare with 1e-3 absolute here
+        assert np.all(np.abs(got - y_w[r]) <= 1e-5 * np.abs(y_w[r]) + 1e-3)
