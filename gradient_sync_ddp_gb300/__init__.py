@@ -240,3 +240,30 @@ __all__ = [
     "version", "lib_handle", "F32", "BF16", "PLAN_CAP", "PLAN_DEEP_FIRST", "FLAG_TREE_ORDER",
     "FLAG_WRITE_BACK_ALL", "FLAG_RING_ORDER", "MAX_REPLICAS",
 ]
+
+
+_lib.syncbn_merge_apply_noalloc.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
+                                            _c.c_int32, _c.c_float, _P, _P, _P, _c.c_int32, _P, _P, _P]
+_lib.syncbn_merge_apply_noalloc.restype = _c.c_int
+_lib.syncbn_noalloc_max_workspace_bytes.argtypes = []
+_lib.syncbn_noalloc_max_workspace_bytes.restype = _c.c_size_t
+
+
+def syncbn_merge_apply_noalloc(xs, ys, mean_out, invstd_out, eps: float = 1e-5, gamma=None, beta=None,
+                               stream=None) -> None:
+    """syncbn_merge_apply for callers that cannot allocate device memory: the
+    statistics scratch is a fixed 1 MiB array inside the library (see
+    include/ddp_sync.h for the size limit, the first-call set-up and why
+    overlapping calls must not run concurrently)."""
+    B, C, H, W = xs[0].shape
+    _check(_lib.syncbn_merge_apply_noalloc(_ptr_array(xs), len(xs), _dtype_code(xs[0]), B, C, H, W, eps,
+                                           _ptr(gamma), _ptr(beta), _ptr_array(ys), _dtype_code(ys[0]),
+                                           _ptr(mean_out), _ptr(invstd_out), _stream_ptr(stream)),
+           "syncbn_merge_apply_noalloc")
+
+
+def syncbn_noalloc_max_workspace_bytes() -> int:
+    return int(_lib.syncbn_noalloc_max_workspace_bytes())
+
+
+__all__ += ["syncbn_merge_apply_noalloc", "syncbn_noalloc_max_workspace_bytes"]

@@ -28,6 +28,7 @@
 //      (the form x·scale + (β − mean·scale) would lose it).
 // Traffic: x is read twice and y written once (2+2+2 bytes per bf16 element).
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "host_common.h"
@@ -361,4 +362,62 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     const bool bf16_out = out_dtype == DDP_BF16;
     if (bf16_in) return bf16_out ? launch_apply<true, true>(p, cvec, nc, agrid, s) : launch_apply<true, false>(p, cvec, nc, agrid, s);
     return bf16_out ? launch_apply<false, true>(p, cvec, nc, agrid, s) : launch_apply<false, false>(p, cvec, nc, agrid, s);
+}
+
+// ---------------------------------------------------------------- variant without a caller workspace
+//
+// Some callers cannot hand this library a workspace because they cannot
+// allocate device memory themselves: code embedded in a host framework whose
+// memory pool owns the whole device and forbids side allocations, code run
+// under a fixed device-memory budget reserved up front, or step loops where
+// cudaMalloc's implicit device synchronisation is not acceptable.  For them
+// the statistics scratch lives in a fixed array compiled into this library.
+namespace ddp {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;   // 1 MiB per device that loads the library
+
+__device__ __align__(256) unsigned char g_syncbn_scratch[kStaticScratchBytes];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of g_syncbn_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in, so the address is looked up once
+// per device (with that device current) and cached.
+int static_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxScratchDevices) return DDP_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_syncbn_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return DDP_OK;
+}
+
+}  // namespace
+}  // namespace ddp
+
+extern "C" size_t syncbn_noalloc_max_workspace_bytes(void) { return ddp::kStaticScratchBytes; }
+
+extern "C" int syncbn_merge_apply_noalloc(const void* const* x, int32_t n_replicas, int32_t in_dtype,
+                                          int32_t batch, int32_t C, int32_t H, int32_t W, float eps,
+                                          const float* gamma, const float* beta,
+                                          void* const* y, int32_t out_dtype, float* mean_out, float* invstd_out,
+                                          void* stream) {
+    const size_t need = syncbn_workspace_bytes(n_replicas, batch, C, H, W);
+    if (need == 0) return DDP_ERR_INVALID_ARG;
+    if (need > ddp::kStaticScratchBytes) return DDP_ERR_CAPACITY;
+    void* ws = nullptr;
+    const int st = ddp::static_scratch(&ws);
+    if (st != DDP_OK) return st;
+    return syncbn_merge_apply(x, n_replicas, in_dtype, batch, C, H, W, eps, gamma, beta, y, out_dtype, mean_out,
+                              invstd_out, ws, ddp::kStaticScratchBytes, stream);
 }

@@ -216,6 +216,40 @@ int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtyp
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * syncbn_merge_apply_noalloc — syncbn_merge_apply without a caller workspace.
+ *
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory themselves (code inside a host framework
+ * whose memory pool owns the device and forbids side allocations, code under
+ * a device-memory budget fixed up front, step loops that cannot afford
+ * cudaMalloc's implicit device synchronisation).  It allocates nothing and
+ * frees nothing; its scratch is a fixed array of
+ * syncbn_noalloc_max_workspace_bytes() bytes (1 MiB) compiled into the
+ * library, held by every GPU that loads the library until the process exits.
+ *
+ *   Arguments, results and errors are those of syncbn_merge_apply, without
+ *   workspace/workspace_bytes.  Sizes whose syncbn_workspace_bytes(...)
+ *   exceeds the fixed array are rejected with DDP_ERR_CAPACITY (every shape
+ *   with C <= 32768 fits; C <= 2048 needs at most 96 KiB).
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress, with that device current) and caches it;
+ *   make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents (nothing in it needs to start at zero).  Calls whose
+ *   kernels overlap on the GPU (different streams without ordering between
+ *   them) race on the array and give wrong results; order them on one stream
+ *   or with events.
+ */
+int syncbn_merge_apply_noalloc(const void* const* x, int32_t n_replicas, int32_t in_dtype,
+                               int32_t batch, int32_t C, int32_t H, int32_t W, float eps,
+                               const float* gamma, const float* beta,
+                               void* const* y, int32_t out_dtype, float* mean_out, float* invstd_out,
+                               void* stream);
+
+/* Size in bytes of the fixed scratch array used by syncbn_merge_apply_noalloc. */
+size_t syncbn_noalloc_max_workspace_bytes(void);
+
+/*
  * dist_sampler_num_samples — indices per rank ([DDP] §4.4):
  * floor(n/N) with drop_last, else ceil(n/N).  -1 on invalid input.
  */
