@@ -5,9 +5,9 @@ Headline workload (one "step" = one pass of the gradient-sync hot path):
 ResNet-50 parameter layout (161 tensors, 25,557,032 fp32 elements), 8
 replicas' gradients resident in HBM, planned into 25 MiB buckets in reverse
 registration order (5 buckets), each bucket averaged by one
-ddp_bucket_allreduce_mean launch.  Each bucket's launch is captured once as
-its own CUDA Graph on a side stream (as per-bucket communication graphs are
-captured once and replayed); a step replays the 5 graphs.
+ddp_bucket_allreduce_mean launch.  The step's 5 per-bucket launches are
+captured once into a CUDA Graph on a side stream, so a step's host dispatch
+is one graph launch; the timed region replays it K times.
 
 Metric: algorithmic HBM bytes moved per second, (N+1)*4 bytes per element
 (N replica reads + one fp32 write), and that rate as a fraction of the
@@ -143,15 +143,17 @@ def summarize_clocks(rows, t0, t1):
             "power_w_max": max(pw) if pw else None}
 
 
-def profile_traffic(source_files):
-    """ncu DRAM bytes per launch of the dominant kernel, from the committed
-    summary, if the kernel's sources still hash to what was profiled."""
+def profile_traffic(source_files, elems_per_launch):
+    """ncu DRAM bytes per launch of the dominant kernel: the committed
+    summary's bytes per element (measured on one launch of the same kernel)
+    times the elements of an average launch here, or None if the kernel's
+    sources no longer hash to what was profiled."""
     path = os.path.join(ROOT, "profiles", "mean_kernel_resnet50.md")
     try:
         txt = open(path, encoding="utf-8").read()
     except OSError:
         return None, None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+source_sha256:\s*([0-9a-f]+)", txt)
+    m = re.search(r"traffic_bytes_per_element:\s*([0-9.eE+]+)\s+source_sha256:\s*([0-9a-f]+)", txt)
     if not m:
         return None, None
     h = hashlib.sha256()
@@ -160,12 +162,12 @@ def profile_traffic(source_files):
             h.update(fh.read())
     if h.hexdigest()[:16] != m.group(2)[:16]:
         return None, "kernel changed since the ncu capture"
-    return float(m.group(1)), None
+    return float(m.group(1)) * elems_per_launch, None
 
 
 def kernel_source_hash():
     csrc = os.path.join(ROOT, "gradient_sync_ddp_gb300", "csrc")
-    return [os.path.join(csrc, f) for f in ("allreduce.cu", "common.cuh")]
+    return [os.path.join(csrc, f) for f in ("allreduce.cu", "common.cuh", "host_common.h")]
 
 
 # ----------------------------------------------------------------------------- workload
@@ -297,32 +299,29 @@ def run_ours(args, world, rank, local):
         off, n = buckets[b][0], buckets[b][1]
         g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps], out[off:off + n])
 
-    # capture one graph per bucket on the side stream
+    # capture one step (the 5 bucket launches, in bucket order) as one graph on the side stream
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
         for b in range(len(buckets)):
             launch(b)
     torch.cuda.synchronize()
-    graphs = []
-    for b in range(len(buckets)):
-        gr = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gr, stream=side):
+    step_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(step_graph, stream=side):
+        for b in range(len(buckets)):
             launch(b)
-        graphs.append(gr)
     torch.cuda.synchronize()
 
     step_bytes = algorithmic_bytes(plan)
     bucket_bytes = [(N_REPLICAS + 1) * 4 * b[1] for b in buckets]
-    nb = len(graphs)
+    nb = len(buckets)
     K, W = args.steps, args.warmup
 
     with torch.cuda.stream(side):
         for _ in range(W):
-            for gr in graphs:
-                gr.replay()
+            step_graph.replay()
     torch.cuda.synchronize()
 
-    events = [torch.cuda.Event(enable_timing=True) for _ in range(K * nb + 1)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
@@ -332,33 +331,42 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     t_host0 = time.time()
     with torch.cuda.stream(side):
-        events[0].record()
-        i = 1
+        t_start.record()
         for _ in range(K):
-            for gr in graphs:
-                gr.replay()
-                events[i].record()
-                i += 1
+            step_graph.replay()
+        t_end.record()
     torch.cuda.synchronize()
     t_host1 = time.time()
     if world > 1:
         dist.barrier()
     clock_rows = sampler.stop() if rank == 0 else []
-    elapsed_ms = events[0].elapsed_time(events[-1])
-    dur = [events[j].elapsed_time(events[j + 1]) for j in range(K * nb)]   # per launch, ms
-    elapsed = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    local_ms = t_start.elapsed_time(t_end)
+    elapsed = torch.tensor([local_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
     elapsed_ms = float(elapsed.item())
     value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
 
-    # per-launch roofline of the averaging kernel over the timed region
-    sum_dur = [0.0] * nb
-    for j, d in enumerate(dur):
-        sum_dur[j % nb] += d
-    achieved = sum(bucket_bytes) * K / (sum(sum_dur) * 1e-3) / 1e9
+    # The timed region runs nothing but the averaging kernel (K x 5 launches
+    # back to back), so its average launch duration is the region time over
+    # the launches, on this rank's stream.
+    avg_launch_ms = local_ms / (K * nb)
+    achieved = (step_bytes / nb) / (avg_launch_ms * 1e-3) / 1e9
     peak, peak_kind = load_peak()
-    traffic, traffic_note = profile_traffic(kernel_source_hash())
+    traffic, traffic_note = profile_traffic(kernel_source_hash(), step_bytes / nb / ((N_REPLICAS + 1) * 4))
+
+    # diagnostic (not the headline): each bucket's launch timed on its own, eagerly
+    per_bucket_us = []
+    with torch.cuda.stream(side):
+        for b in range(nb):
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record()
+            for _ in range(20):
+                launch(b)
+            eb.record()
+            per_bucket_us.append((ea, eb))
+    torch.cuda.synchronize()
+    per_bucket_us = [ea.elapsed_time(eb) / 20 * 1e3 for ea, eb in per_bucket_us]
 
     # end to end through the public API: pinned host replicas -> HBM, 5 bucket calls, result -> pinned host
     host_reps = [torch.empty(total, dtype=torch.float32, pin_memory=True) for _ in range(N_REPLICAS)]
@@ -409,8 +417,10 @@ def run_ours(args, world, rank, local):
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} (HBM copy bandwidth)",
                          "kernel": "mean_kernel (ddp_bucket_allreduce_mean, fp32, rank order, N=8)",
-                         "bytes_per_launch": bucket_bytes,
-                         "avg_launch_us": [s / K * 1e3 for s in sum_dur],
+                         "algorithmic_bytes_per_launch": step_bytes / nb,
+                         "avg_launch_us": avg_launch_ms * 1e3,
+                         "per_bucket_bytes": bucket_bytes,
+                         "per_bucket_us_eager_diagnostic": per_bucket_us,
                          **({"traffic_note": traffic_note} if traffic_note else {})},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": N_REPLICAS * total * 4,

@@ -12,8 +12,10 @@
 // each thread streams one 16-byte vector from every replica (all N loads are
 // issued before the first add, N*16 bytes in flight per thread), keeps the
 // adds in the exact rank order with __fadd_rn (no contraction), and writes
-// the fp32 result with a streaming store.  The grid is a multiple of the SM
-// count (resident blocks per SM x SMs) and strides over the bucket.  The
+// the fp32 result with a streaming store.  The grid is exactly one wave
+// (resident CTAs per SM from the occupancy calculator x SMs) and strides over
+// the bucket, so no partial last wave idles SMs; launches use programmatic
+// dependent launch so back-to-back bucket kernels overlap launch and tail.  The
 // replica pointers travel in a __grid_constant__ parameter block, so a
 // launch is self-contained and capturable into a CUDA Graph.
 #include <cstdint>
@@ -88,6 +90,7 @@ __global__ void __launch_bounds__(kThreads) mean_kernel(const __grid_constant__ 
     const int64_t nvec = a.numel / VEC;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    pdl_enter();
 
     for (int64_t v = gtid; v < nvec; v += stride) {
         const int64_t e0 = v * VEC;
@@ -206,6 +209,7 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
     const int64_t nvec = a.numel / VEC;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    pdl_enter();
 
     for (int64_t v = gtid; v < nvec; v += stride) {
         const int64_t e0 = v * VEC;
@@ -257,56 +261,53 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
 
 // ---------------------------------------------------------------- host side
 
-int launch_grid(int64_t nvec, int* grid) {
-    DeviceInfo d;
-    int st = current_device_info(&d);
+// One wave of CTAs for a bucket of nvec 16-byte vectors, then a PDL launch.
+template <typename Params>
+int launch_wave(void (*kernel)(Params), int64_t nvec, cudaStream_t s, const Params& p) {
+    int grid = 0;
+    const int st = one_wave_grid(reinterpret_cast<const void*>(kernel), kThreads,
+                                 (nvec + kThreads - 1) / kThreads, &grid);
     if (st != DDP_OK) return st;
-    const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
-    int64_t need = (nvec + kThreads - 1) / kThreads;
-    if (need < 1) need = 1;   // block 0 also covers the ragged tail
-    *grid = static_cast<int>(need < resident ? need : resident);
-    return DDP_OK;
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), kThreads, s, p);
 }
 
 template <int NMAX, bool BF16, int ORDER, bool WB, bool NC>
-int launch_mean(const MeanParams& p, int grid, cudaStream_t s) {
-    mean_kernel<NMAX, BF16, ORDER, WB, NC><<<grid, kThreads, 0, s>>>(p);
-    return check_launch();
+int launch_mean(const MeanParams& p, int64_t nvec, cudaStream_t s) {
+    return launch_wave(mean_kernel<NMAX, BF16, ORDER, WB, NC>, nvec, s, p);
 }
 
 template <int NMAX, bool BF16, int ORDER>
-int dispatch_mean_mode(const MeanParams& p, int grid, cudaStream_t s, bool wb, bool aliased) {
+int dispatch_mean_mode(const MeanParams& p, int64_t nvec, cudaStream_t s, bool wb, bool aliased) {
     if constexpr (BF16) {
-        return launch_mean<NMAX, true, ORDER, false, true>(p, grid, s);
+        return launch_mean<NMAX, true, ORDER, false, true>(p, nvec, s);
     } else {
-        if (wb) return launch_mean<NMAX, false, ORDER, true, false>(p, grid, s);
-        if (aliased) return launch_mean<NMAX, false, ORDER, false, false>(p, grid, s);
-        return launch_mean<NMAX, false, ORDER, false, true>(p, grid, s);
+        if (wb) return launch_mean<NMAX, false, ORDER, true, false>(p, nvec, s);
+        if (aliased) return launch_mean<NMAX, false, ORDER, false, false>(p, nvec, s);
+        return launch_mean<NMAX, false, ORDER, false, true>(p, nvec, s);
     }
 }
 
 template <int NMAX, bool BF16>
-int dispatch_mean_order(const MeanParams& p, int grid, cudaStream_t s, int order, bool wb, bool aliased) {
+int dispatch_mean_order(const MeanParams& p, int64_t nvec, cudaStream_t s, int order, bool wb, bool aliased) {
     switch (order) {
-        case kTree: return dispatch_mean_mode<NMAX, BF16, kTree>(p, grid, s, wb, aliased);
-        case kRing: return dispatch_mean_mode<NMAX, BF16, kRing>(p, grid, s, wb, aliased);
-        default: return dispatch_mean_mode<NMAX, BF16, kRank>(p, grid, s, wb, aliased);
+        case kTree: return dispatch_mean_mode<NMAX, BF16, kTree>(p, nvec, s, wb, aliased);
+        case kRing: return dispatch_mean_mode<NMAX, BF16, kRing>(p, nvec, s, wb, aliased);
+        default: return dispatch_mean_mode<NMAX, BF16, kRank>(p, nvec, s, wb, aliased);
     }
 }
 
 template <bool BF16>
-int dispatch_mean(const MeanParams& p, int grid, cudaStream_t s, int order, bool wb, bool aliased) {
-    if (p.n <= 4) return dispatch_mean_order<4, BF16>(p, grid, s, order, wb, aliased);
-    if (p.n <= 8) return dispatch_mean_order<8, BF16>(p, grid, s, order, wb, aliased);
-    return dispatch_mean_order<16, BF16>(p, grid, s, order, wb, aliased);
+int dispatch_mean(const MeanParams& p, int64_t nvec, cudaStream_t s, int order, bool wb, bool aliased) {
+    if (p.n <= 4) return dispatch_mean_order<4, BF16>(p, nvec, s, order, wb, aliased);
+    if (p.n <= 8) return dispatch_mean_order<8, BF16>(p, nvec, s, order, wb, aliased);
+    return dispatch_mean_order<16, BF16>(p, nvec, s, order, wb, aliased);
 }
 
 template <bool BF16>
-int dispatch_sgd(const SgdParams& p, int grid, cudaStream_t s) {
-    if (p.n <= 4) sgd_kernel<4, BF16><<<grid, kThreads, 0, s>>>(p);
-    else if (p.n <= 8) sgd_kernel<8, BF16><<<grid, kThreads, 0, s>>>(p);
-    else sgd_kernel<16, BF16><<<grid, kThreads, 0, s>>>(p);
-    return check_launch();
+int dispatch_sgd(const SgdParams& p, int64_t nvec, cudaStream_t s) {
+    if (p.n <= 4) return launch_wave(sgd_kernel<4, BF16>, nvec, s, p);
+    if (p.n <= 8) return launch_wave(sgd_kernel<8, BF16>, nvec, s, p);
+    return launch_wave(sgd_kernel<16, BF16>, nvec, s, p);
 }
 
 bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
@@ -368,12 +369,10 @@ extern "C" int ddp_bucket_allreduce_mean(const void* const* replicas, int32_t n_
     p.ring_base = numel / n_replicas;
     p.ring_rem = numel % n_replicas;
     const int order = tree ? kTree : ring ? kRing : kRank;
-    const int vec = in_dtype == DDP_BF16 ? 8 : 4;
-    int grid = 0;
-    if ((st = launch_grid(numel / vec, &grid)) != DDP_OK) return st;
+    const int64_t nvec = numel / (in_dtype == DDP_BF16 ? 8 : 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return in_dtype == DDP_BF16 ? dispatch_mean<true>(p, grid, s, order, wb, aliased)
-                                : dispatch_mean<false>(p, grid, s, order, wb, aliased);
+    return in_dtype == DDP_BF16 ? dispatch_mean<true>(p, nvec, s, order, wb, aliased)
+                                : dispatch_mean<false>(p, nvec, s, order, wb, aliased);
 }
 
 extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
@@ -413,8 +412,7 @@ extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_r
     p.lr = lr;
     p.mom = momentum;
     p.wd = weight_decay;
-    int grid = 0;
-    if ((st = launch_grid(numel / (in_dtype == DDP_BF16 ? 8 : 4), &grid)) != DDP_OK) return st;
+    const int64_t nvec = numel / (in_dtype == DDP_BF16 ? 8 : 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return in_dtype == DDP_BF16 ? dispatch_sgd<true>(p, grid, s) : dispatch_sgd<false>(p, grid, s);
+    return in_dtype == DDP_BF16 ? dispatch_sgd<true>(p, nvec, s) : dispatch_sgd<false>(p, nvec, s);
 }

@@ -66,6 +66,18 @@ __device__ __forceinline__ float load_elem(const void* base, int64_t e) {
     }
 }
 
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialisation allowed, so its launch (and the
+// scheduling of its CTAs on SMs freed by the previous kernel) overlaps the
+// tail of the kernel before it on the stream.  Correctness does not depend on
+// what that previous kernel was: each kernel first lets its own dependents
+// launch, then waits for the full completion (and memory flush) of the grid
+// it depends on before it touches global memory.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace ddp
 
 namespace ddp {

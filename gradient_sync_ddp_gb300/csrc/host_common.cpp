@@ -1,7 +1,9 @@
 // Status strings, thread-local CUDA error and the per-device launch-limit cache.
 #include "host_common.h"
 
+#include <map>
 #include <mutex>
+#include <utility>
 
 namespace ddp {
 
@@ -42,6 +44,26 @@ int current_device_info(DeviceInfo* out) {
         g_info_valid[dev] = true;
     }
     *out = g_info[dev];
+    return DDP_OK;
+}
+
+int resident_blocks_per_sm(const void* func, int block, int* out) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> cache;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_pair(func, dev * 4096 + block);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, block, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (n < 1) n = 1;
+        it = cache.emplace(key, n).first;
+    }
+    *out = it->second;
     return DDP_OK;
 }
 

@@ -151,12 +151,11 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     p.rank = rank;
     p.shuffle = shuffle;
 
-    DeviceInfo d;
-    int st = current_device_info(&d);
+    int grid = 0;
+    const int st = one_wave_grid(reinterpret_cast<const void*>(sampler_kernel), kThreads,
+                                 (count + kThreads - 1) / kThreads, &grid);
     if (st != DDP_OK) return st;
-    const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
-    int64_t grid = (count + kThreads - 1) / kThreads;
-    if (grid > resident) grid = resident;
-    sampler_kernel<<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    // plain launch: the status word's memset just before must complete first
+    sampler_kernel<<<grid, kThreads, 0, s>>>(p);
     return check_launch();
 }

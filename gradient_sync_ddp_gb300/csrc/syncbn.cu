@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constan
     const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
     const uint32_t units = static_cast<uint32_t>(a.HW / W);     // accesses per plane
     const uint32_t total = static_cast<uint32_t>(p1 - p0) * units;
+    pdl_enter();
 
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
     float acc_s = 0.0f, acc_q = 0.0f;
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constan
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) bn_merge_kernel(const __grid_constant__ BnParams a) {
     const int c = blockIdx.x * kThreads + threadIdx.x;
+    pdl_enter();
     if (c >= a.C) return;
     double S = 0.0, Q = 0.0;
     for (int s = 0; s < a.S; ++s) {
@@ -174,6 +176,7 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
     const uint32_t nvec = E / 8;
     const uint32_t stride = gridDim.x * kThreads;
     const uint32_t gtid = blockIdx.x * kThreads + threadIdx.x;
+    pdl_enter();
     for (uint32_t v = gtid; v < nvec; v += stride) {
         const uint32_t e0 = v * 8;
         float xv[8];
@@ -250,13 +253,11 @@ bool valid_sizes(int32_t n, int32_t batch, int32_t C, int32_t H, int32_t W) {
 template <bool BF16_IN, bool BF16_OUT>
 int launch_apply(const BnParams& p, bool cvec, bool nc, dim3 grid, cudaStream_t s) {
     if (cvec) {
-        if (nc) bn_apply_kernel<BF16_IN, BF16_OUT, true, true><<<grid, kThreads, 0, s>>>(p);
-        else bn_apply_kernel<BF16_IN, BF16_OUT, true, false><<<grid, kThreads, 0, s>>>(p);
-    } else {
-        if (nc) bn_apply_kernel<BF16_IN, BF16_OUT, false, true><<<grid, kThreads, 0, s>>>(p);
-        else bn_apply_kernel<BF16_IN, BF16_OUT, false, false><<<grid, kThreads, 0, s>>>(p);
+        if (nc) return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, true, true>, grid, kThreads, s, p);
+        return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, true, false>, grid, kThreads, s, p);
     }
-    return check_launch();
+    if (nc) return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, false, true>, grid, kThreads, s, p);
+    return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, false, false>, grid, kThreads, s, p);
 }
 
 }  // namespace
@@ -335,18 +336,16 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const dim3 sgrid(static_cast<unsigned>(C), static_cast<unsigned>(p.S));
-    if (bf16_in) {
-        if (vec) bn_stats_kernel<true, true><<<sgrid, kThreads, 0, s>>>(p);
-        else bn_stats_kernel<true, false><<<sgrid, kThreads, 0, s>>>(p);
-    } else {
-        if (vec) bn_stats_kernel<false, true><<<sgrid, kThreads, 0, s>>>(p);
-        else bn_stats_kernel<false, false><<<sgrid, kThreads, 0, s>>>(p);
-    }
-    int st = check_launch();
+    int st;
+    if (bf16_in) st = vec ? launch_pdl(bn_stats_kernel<true, true>, sgrid, kThreads, s, p)
+                          : launch_pdl(bn_stats_kernel<true, false>, sgrid, kThreads, s, p);
+    else st = vec ? launch_pdl(bn_stats_kernel<false, true>, sgrid, kThreads, s, p)
+                  : launch_pdl(bn_stats_kernel<false, false>, sgrid, kThreads, s, p);
     if (st != DDP_OK) return st;
-    if (bf16_in) bn_merge_kernel<true><<<(C + kThreads - 1) / kThreads, kThreads, 0, s>>>(p);
-    else bn_merge_kernel<false><<<(C + kThreads - 1) / kThreads, kThreads, 0, s>>>(p);
-    if ((st = check_launch()) != DDP_OK) return st;
+    const dim3 mgrid(static_cast<unsigned>((C + kThreads - 1) / kThreads));
+    st = bf16_in ? launch_pdl(bn_merge_kernel<true>, mgrid, kThreads, s, p)
+                 : launch_pdl(bn_merge_kernel<false>, mgrid, kThreads, s, p);
+    if (st != DDP_OK) return st;
 
     DeviceInfo d;
     if ((st = current_device_info(&d)) != DDP_OK) return st;
