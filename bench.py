@@ -436,16 +436,26 @@ def run_ours(args, world, rank, local):
 
 
 def _time_launches(torch, fn, iters, stream):
-    """Mean device time (ms) of fn() over iters launches on stream, after 3 warm-ups."""
+    """Mean device time (ms) of one fn() call: fn's launches are captured once
+    into a CUDA Graph on `stream` (after 3 eager warm-up calls) and the graph
+    is replayed 3 times untimed, then `iters` times between two events, so
+    host dispatch cost is not part of the figure."""
     with torch.cuda.stream(stream):
         for _ in range(3):
             fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         a.record()
         for _ in range(iters):
-            fn()
+            graph.replay()
         b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / iters

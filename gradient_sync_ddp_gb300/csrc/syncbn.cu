@@ -7,25 +7,41 @@
 // of the whole global batch (one extra all-reduce per BN layer).
 //
 // Three launches on the caller's stream:
-//   1. stats  — grid (C, S): CTA (c, s) reduces slice s of the N*batch planes
-//      of channel c (each plane is H*W contiguous elements of one replica and
-//      one sample).  Threads stream 16-byte vectors when a plane's length is
-//      a multiple of the vector width, single elements otherwise.  The sums
-//      are shifted by K_c, the channel's first element (replica 0, sample 0):
-//      d = x − K_c, and Σd, Σd² are accumulated, so Q/M − mean² never
-//      subtracts two large nearly equal numbers when |mean| >> std.  Each
-//      vector is summed pairwise in fp32, a thread accumulates at most a few
-//      hundred elements in fp32, and the CTA combines its threads in fp64
-//      into workspace partials.
-//   2. merge  — one thread per channel sums the S partials in fixed order in
+//   1. stats  — per-channel partial sums over slices of the N*batch samples.
+//      The sums are shifted by K_c, the channel's first element (replica 0,
+//      sample 0): d = x − K_c, and Σd, Σd² are accumulated, so Q/M − mean²
+//      never subtracts two large nearly equal numbers when |mean| >> std.
+//      The kernel depends on the plane (H*W contiguous elements of one
+//      sample and channel):
+//        plane kernel — H*W a multiple of the 16-byte vector (56x56, 28x28):
+//          CTA (c, s) streams its planes with 16-byte loads.
+//        segment kernel — unaligned planes at least one vector long (7x7,
+//          14x14, 3x3): a CTA owns G consecutive channels (G*H*W about 2K
+//          elements) and a slice of the samples; for one sample those G
+//          channels are one contiguous run, read as the aligned 16-byte
+//          vectors that cover it.  A vector spans at most two channels, so a
+//          thread reduces it to two (Σd, Σd²) segments in shared memory, and
+//          one thread per (sample, channel) then adds its channel's segments.
+//        staged group kernel — planes shorter than a vector (1x1, 2x2):
+//          runs are copied to shared memory and reduced per channel there.
+//      Every kernel reads a run's ragged end element by element, so no
+//      access leaves the replica buffer.
+//      Threads accumulate at most a few hundred elements in fp32 (vectors
+//      summed pairwise); the CTA combines threads in float-float (pairs of
+//      fp32, ~48 significant bits: GB300's fp64 pipe is too narrow for
+//      reductions) and stores one fp32 (sum, sum of squares) partial per
+//      channel and slice.
+//   2. merge  — one warp per channel sums the S partials in a fixed order in
+//      float-float (fp32 pairs), then one thread per channel finalises in
 //      fp64: with m' = Σd/M, mean = K_c + m', var = Σd²/M − m'² (the same
 //      S/M and Q/M − mean² up to rounding), invstd = 1/sqrt(var + eps); it
 //      stores per channel (m_hi, m_lo, scale, β) where m_hi + m_lo is the
 //      mean as an fp32 pair and scale = invstd·γ.
 //   3. apply  — y = ((x − m_hi) − m_lo)·scale + β over every replica, 16-byte
-//      vectors in and out.  x − m_hi is exact when x is near the mean
-//      (Sterbenz), so no cancellation error is amplified by a large invstd
-//      (the form x·scale + (β − mean·scale) would lose it).
+//      vectors in and out, the channel computed once per 8-element vector.
+//      x − m_hi is exact when x is near the mean (Sterbenz), so no
+//      cancellation error is amplified by a large invstd (the form
+//      x·scale + (β − mean·scale) would lose it).
 // Traffic: x is read twice and y written once (2+2+2 bytes per bf16 element).
 #include <cstdint>
 #include <mutex>
@@ -36,7 +52,10 @@
 namespace ddp {
 namespace {
 
-constexpr int kTargetCtas = 2048;   // stats CTAs aimed for (~1.7 waves of 8 CTAs on 152 SMs)
+constexpr int kTargetCtas = 2048;        // stats CTAs aimed for (about two waves on 152 SMs)
+constexpr int64_t kMaxPartials = 65536;  // C*S bound: fp32 partials stay <= 512 KiB
+constexpr int kRunElems = 2048;          // channels per group: G*H*W <= this (G >= 1)
+constexpr int kStageBytes = 24576;       // shared staging per group-kernel CTA
 
 struct BnParams {
     const void* x[DDP_MAX_REPLICAS];
@@ -45,22 +64,48 @@ struct BnParams {
     const float* beta;
     float* mean_out;
     float* invstd_out;
-    double2* partial;   // [C][S] (sum, sum of squares)
+    float2* partial;    // [C][S] (Σd, Σd²) per channel and slice
     float4* coef;       // [C] (m_hi, m_lo, scale, beta)
-    FastDiv div_unit;   // per-plane unit count (vectors or elements per plane)
+    FastDiv div_unit;   // plane kernel: accesses per plane; group kernel: 16-byte vectors per staging slot
     FastDiv div_batch;  // batch
     FastDiv div_hw;     // H*W
     FastDiv div_c;      // C
     int32_t n, batch, C, HW, S;
+    int32_t G;          // group kernel: channels per CTA (power of two)
+    int32_t R;          // group kernel: runs staged per tile
+    int32_t slot_bytes; // group kernel: shared bytes per staged run
     float eps;
 };
 
-__device__ __forceinline__ void block_sum2(double& a, double& b) {
-    __shared__ double sh[2][kThreads / 32];
+// Float-float arithmetic: a value is hi + lo, kept with fp32 operations only
+// (Knuth's TwoSum, then a renormalising Fast2Sum), about 48 significant bits.
+// GB300's FP64 pipe is narrow (one 32-lane fp64 instruction occupies it for
+// many cycles), so the reductions here avoid fp64 and use this instead; the
+// order of every reduction is fixed, so results are deterministic.
+struct FF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float bb = __fsub_rn(s, a.hi);
+    const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+    const float t = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    const float hi = __fadd_rn(s, t);
+    return FF{hi, __fsub_rn(t, __fsub_rn(hi, s))};
+}
+
+__device__ __forceinline__ FF ff_shfl_down(FF v, int o) {
+    return FF{__shfl_down_sync(0xffffffffu, v.hi, o), __shfl_down_sync(0xffffffffu, v.lo, o)};
+}
+
+// Sum of two per-thread values over the CTA in float-float, result in thread 0.
+__device__ __forceinline__ void block_sum2_ff(FF& a, FF& b) {
+    __shared__ FF sh[2][kThreads / 32];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        a += __shfl_down_sync(0xffffffffu, a, o);
-        b += __shfl_down_sync(0xffffffffu, b, o);
+        a = ff_add(a, ff_shfl_down(a, o));
+        b = ff_add(b, ff_shfl_down(b, o));
     }
     const int w = threadIdx.x / 32, l = threadIdx.x % 32;
     if (l == 0) {
@@ -69,17 +114,233 @@ __device__ __forceinline__ void block_sum2(double& a, double& b) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        a = 0.0;
-        b = 0.0;
-        for (int i = 0; i < kThreads / 32; ++i) {
-            a += sh[0][i];
-            b += sh[1][i];
+        a = sh[0][0];
+        b = sh[1][0];
+        for (int i = 1; i < kThreads / 32; ++i) {
+            a = ff_add(a, sh[0][i]);
+            b = ff_add(b, sh[1][i]);
         }
     }
 }
 
+template <bool BF16>
+__device__ __forceinline__ float shared_elem(const unsigned char* p, int e) {
+    if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(p)[e]) << 16);
+    else return reinterpret_cast<const float*>(p)[e];
+}
+
+// Group kernel, grid (ceil(C/G), S).
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_constant__ BnParams a) {
+    constexpr int ESZ = BF16 ? 2 : 4;
+    __shared__ __align__(16) unsigned char stage[kStageBytes];
+    __shared__ float red[2][kThreads];
+    const int c0 = blockIdx.x * a.G, s = blockIdx.y;
+    const int Gc = min(a.G, a.C - c0);            // channels of this group
+    const int Tc = kThreads / a.G;                // threads per channel
+    const int cl = threadIdx.x / Tc, k = threadIdx.x - cl * Tc;
+    const bool active = cl < Gc;
+    const int P = a.n * a.batch;
+    const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
+    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
+    const uint64_t run_bytes = static_cast<uint64_t>(Gc) * a.HW * ESZ;
+    const uint32_t vslot = static_cast<uint32_t>(a.slot_bytes / 16);
+    pdl_enter();
+    const float K = active ? load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + cl) * a.HW) : 0.0f;
+
+    float acc_s = 0.0f, acc_q = 0.0f;
+    for (int t0 = p0; t0 < p1; t0 += a.R) {
+        const int nr = min(a.R, p1 - t0);
+        // stage runs t0 .. t0+nr-1
+        const uint32_t total = static_cast<uint32_t>(nr) * vslot;
+        for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
+            const uint32_t j = fdiv(t, a.div_unit);
+            const uint32_t v = t - j * vslot;
+            const uint32_t pl = static_cast<uint32_t>(t0) + j;
+            const uint32_t r = fdiv(pl, a.div_batch);
+            const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
+            const char* base = static_cast<const char*>(a.x[r]);
+            const uint64_t a0 = (static_cast<uint64_t>(b) * a.C + c0) * a.HW * ESZ;   // run bytes [a0, a1)
+            const uint64_t a1 = a0 + run_bytes;
+            const uint64_t a0al = a0 & ~uint64_t(15), a1fl = a1 & ~uint64_t(15);
+            const uint64_t src = a0al + 16ull * v;
+            unsigned char* dst = stage + j * a.slot_bytes + 16 * v;
+            if (src < a1fl) {
+                *reinterpret_cast<uint4*>(dst) = ld16<true>(base + src);
+            } else if (src < a1) {                      // ragged end, element by element
+                const uint64_t lo = src > a0 ? src : a0;
+                const uint64_t hi = (src + 16 < a1) ? src + 16 : a1;
+                for (uint64_t q = lo; q < hi; q += ESZ) {
+                    if constexpr (BF16)
+                        *reinterpret_cast<unsigned short*>(stage + j * a.slot_bytes + (q - a0al)) =
+                            *reinterpret_cast<const unsigned short*>(base + q);
+                    else
+                        *reinterpret_cast<float*>(stage + j * a.slot_bytes + (q - a0al)) =
+                            *reinterpret_cast<const float*>(base + q);
+                }
+            }
+        }
+        __syncthreads();
+        if (active) {
+            for (int j = 0; j < nr; ++j) {
+                const uint32_t pl = static_cast<uint32_t>(t0 + j);
+                const uint32_t r = fdiv(pl, a.div_batch);
+                const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
+                const uint32_t pre = static_cast<uint32_t>(((static_cast<uint64_t>(b) * a.C + c0) * a.HW * ESZ) & 15u);
+                const unsigned char* run = stage + j * a.slot_bytes + pre;
+                const int e0 = cl * a.HW;
+                for (int e = k; e < a.HW; e += Tc) {
+                    const float d = __fsub_rn(shared_elem<BF16>(run, e0 + e), K);
+                    acc_s += d;
+                    acc_q += d * d;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    red[0][threadIdx.x] = acc_s;
+    red[1][threadIdx.x] = acc_q;
+    __syncthreads();
+    if (threadIdx.x < Gc) {
+        FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
+        for (int i = 0; i < Tc; ++i) {
+            S = ff_add(S, FF{red[0][threadIdx.x * Tc + i], 0.0f});
+            Q = ff_add(Q, FF{red[1][threadIdx.x * Tc + i], 0.0f});
+        }
+        a.partial[static_cast<int64_t>(c0 + threadIdx.x) * a.S + s] =
+            make_float2(__fadd_rn(S.hi, S.lo), __fadd_rn(Q.hi, Q.lo));
+    }
+}
+
+// Segment kernel, grid (ceil(C/G), S), for H*W >= the vector width W and not
+// a multiple of it (7x7, 14x14, 3x3, ...).  Runs (one sample's G channels)
+// are read as the 16-byte vectors of the aligned grid that covers them, so a
+// vector holds elements of at most two channels of the group (or of the
+// neighbouring groups, which are masked out).  Phase A: each thread turns
+// one vector into (Σd, Σd²) of its first channel and of the next one and
+// stores them in shared memory.  Phase B: thread (run j, channel cl, part k)
+// adds up the segments of channel cl's vectors.  A run's last vector is read
+// element by element where it would extend past the run, so no access
+// leaves the replica buffer.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) bn_stats_segment_kernel(const __grid_constant__ BnParams a) {
+    constexpr int ESZ = BF16 ? 2 : 4;
+    constexpr int W = 16 / ESZ;
+    __shared__ float4 seg[kStageBytes / 16];
+    __shared__ float Ks[kThreads];
+    __shared__ float red[2][kThreads];
+    const int c0 = blockIdx.x * a.G, s = blockIdx.y;
+    const int Gc = min(a.G, a.C - c0);
+    const int HW = a.HW;
+    const int P = a.n * a.batch;
+    const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
+    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
+    const uint32_t vslot = static_cast<uint32_t>(a.slot_bytes / 16);   // vectors per run (upper bound)
+    const uint32_t run_elems = static_cast<uint32_t>(Gc) * HW;
+    // phase-B role: pair (j, cl) and part k of Tk
+    const int Tk = kThreads / (a.R * a.G);
+    const int pair = threadIdx.x / Tk, k = threadIdx.x - pair * Tk;
+    const int jb = pair / a.G, cl = pair - jb * a.G;
+    pdl_enter();
+    if (threadIdx.x < Gc) Ks[threadIdx.x] = load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + threadIdx.x) * HW);
+    __syncthreads();
+
+    float acc_s = 0.0f, acc_q = 0.0f;
+    for (int t0 = p0; t0 < p1; t0 += a.R) {
+        const int nr = min(a.R, p1 - t0);
+        // phase A
+        const uint32_t total = static_cast<uint32_t>(nr) * vslot;
+        for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
+            const uint32_t j = fdiv(t, a.div_unit);
+            const uint32_t v = t - j * vslot;
+            const uint32_t pl = static_cast<uint32_t>(t0) + j;
+            const uint32_t r = fdiv(pl, a.div_batch);
+            const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
+            const uint64_t first = (static_cast<uint64_t>(b) * a.C + c0) * HW;          // run's first element
+            const uint32_t pre = static_cast<uint32_t>(first % W);                      // elements before it in its vector
+            const int32_t e_start = static_cast<int32_t>(v * W) - static_cast<int32_t>(pre);
+            if (e_start >= static_cast<int32_t>(run_elems)) continue;
+            const char* base = static_cast<const char*>(a.x[r]) + (first - pre) * ESZ + 16ull * v;
+            float xe[W];
+            if (e_start + W <= static_cast<int32_t>(run_elems)) {     // the whole vector lies before the run's end
+                const uint4 raw = ld16<true>(base);
+#pragma unroll
+                for (int q = 0; q < W; ++q) xe[q] = vec_elem<BF16>(raw, q);
+            } else {
+#pragma unroll
+                for (int q = 0; q < W; ++q)
+                    xe[q] = (e_start + q < static_cast<int32_t>(run_elems)) ? load_elem<BF16>(base, q) : 0.0f;
+            }
+            const uint32_t e_first = e_start > 0 ? static_cast<uint32_t>(e_start) : 0u;
+            const uint32_t ca = fdiv(e_first, a.div_hw);           // channel (in group) of the first valid element
+            const int32_t eb = static_cast<int32_t>((ca + 1) * HW); // first element of the next channel
+            const float Ka = Ks[ca];
+            const float Kb = (ca + 1 < static_cast<uint32_t>(Gc)) ? Ks[ca + 1] : 0.0f;
+            float sl = 0.0f, ql = 0.0f, sh = 0.0f, qh = 0.0f;
+#pragma unroll
+            for (int q = 0; q < W; ++q) {
+                const int32_t e = e_start + q;
+                const bool valid = e >= 0 && e < static_cast<int32_t>(run_elems);
+                const bool hi = e >= eb;
+                const float d = valid ? __fsub_rn(xe[q], hi ? Kb : Ka) : 0.0f;
+                if (hi) {
+                    sh += d;
+                    qh += d * d;
+                } else {
+                    sl += d;
+                    ql += d * d;
+                }
+            }
+            seg[j * vslot + v] = make_float4(sl, ql, sh, qh);
+        }
+        __syncthreads();
+        // phase B
+        if (jb < nr && cl < Gc) {
+            const uint64_t first = [&] {
+                const uint32_t pl = static_cast<uint32_t>(t0 + jb);
+                const uint32_t r = fdiv(pl, a.div_batch);
+                const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
+                return (static_cast<uint64_t>(b) * a.C + c0) * HW;
+            }();
+            const uint32_t pre = static_cast<uint32_t>(first % W);
+            const uint32_t lo = pre + static_cast<uint32_t>(cl) * HW;       // element position in the vector grid
+            const uint32_t hi = lo + HW - 1;
+            for (uint32_t v = lo / W + k; v <= hi / W; v += Tk) {
+                const int32_t e_start = static_cast<int32_t>(v * W) - static_cast<int32_t>(pre);
+                const uint32_t e_first = e_start > 0 ? static_cast<uint32_t>(e_start) : 0u;
+                const float4 sg = seg[jb * vslot + v];
+                if (fdiv(e_first, a.div_hw) == static_cast<uint32_t>(cl)) {
+                    acc_s += sg.x;
+                    acc_q += sg.y;
+                } else {
+                    acc_s += sg.z;
+                    acc_q += sg.w;
+                }
+            }
+        }
+        __syncthreads();
+    }
+    red[0][threadIdx.x] = acc_s;
+    red[1][threadIdx.x] = acc_q;
+    __syncthreads();
+    if (threadIdx.x < Gc) {
+        FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
+        for (int j = 0; j < a.R; ++j)
+            for (int q = 0; q < Tk; ++q) {
+                const int t = (j * a.G + threadIdx.x) * Tk + q;
+                S = ff_add(S, FF{red[0][t], 0.0f});
+                Q = ff_add(Q, FF{red[1][t], 0.0f});
+            }
+        a.partial[static_cast<int64_t>(c0 + threadIdx.x) * a.S + s] =
+            make_float2(__fadd_rn(S.hi, S.lo), __fadd_rn(Q.hi, Q.lo));
+    }
+}
+
+// Plane kernel, grid (C, S).  VEC: H*W is a multiple of the 16-byte vector
+// width (16-byte loads); otherwise single-element loads (only for planes too
+// large to stage and not vector aligned).
 template <bool BF16, bool VEC>
-__global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constant__ BnParams a) {
+__global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_constant__ BnParams a) {
     constexpr int W = VEC ? (BF16 ? 8 : 4) : 1;    // elements per access
     constexpr int ESZ = BF16 ? 2 : 4;
     const int c = blockIdx.x, s = blockIdx.y;
@@ -89,69 +350,116 @@ __global__ void __launch_bounds__(kThreads) bn_stats_kernel(const __grid_constan
     const uint32_t units = static_cast<uint32_t>(a.HW / W);     // accesses per plane
     const uint32_t total = static_cast<uint32_t>(p1 - p0) * units;
     pdl_enter();
-
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
     float acc_s = 0.0f, acc_q = 0.0f;
-    for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
-        const uint32_t pl_off = fdiv(t, a.div_unit);
-        const uint32_t u = t - pl_off * units;
-        const uint32_t pl = static_cast<uint32_t>(p0) + pl_off;
-        const uint32_t r = fdiv(pl, a.div_batch);
-        const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
-        const int64_t elem = (static_cast<int64_t>(b) * a.C + c) * a.HW + static_cast<int64_t>(u) * W;
-        const char* p = static_cast<const char*>(a.x[r]) + elem * ESZ;
-        if constexpr (VEC) {
-            const uint4 raw = ld16<true>(p);
-            float e[W], q[W];
+    // 4 independent accesses per thread per iteration keep enough bytes in flight
+    for (uint32_t t0 = threadIdx.x; t0 < total; t0 += 4 * kThreads) {
+        uint4 raw[4];
+        float sc[4];
 #pragma unroll
-            for (int k = 0; k < W; ++k) {
-                e[k] = __fsub_rn(vec_elem<BF16>(raw, k), K);
-                q[k] = e[k] * e[k];
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t t = t0 + u * kThreads;
+            raw[u] = make_uint4(0, 0, 0, 0);
+            sc[u] = 0.0f;
+            if (t < total) {
+                const uint32_t pl_off = fdiv(t, a.div_unit);
+                const uint32_t uu = t - pl_off * units;
+                const uint32_t pl = static_cast<uint32_t>(p0) + pl_off;
+                const uint32_t r = fdiv(pl, a.div_batch);
+                const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
+                const int64_t elem = (static_cast<int64_t>(b) * a.C + c) * a.HW + static_cast<int64_t>(uu) * W;
+                const char* ptr = static_cast<const char*>(a.x[r]) + elem * ESZ;
+                if constexpr (VEC) raw[u] = ld16<true>(ptr);
+                else sc[u] = load_elem<BF16>(ptr, 0);
             }
+        }
 #pragma unroll
-            for (int w = W; w > 1; w >>= 1)
+        for (int u = 0; u < 4; ++u) {
+            if (t0 + u * kThreads >= total) continue;
+            if constexpr (VEC) {
+                float e[W], q[W];
 #pragma unroll
-                for (int k = 0; k < w / 2; ++k) {
-                    e[k] = e[2 * k] + e[2 * k + 1];
-                    q[k] = q[2 * k] + q[2 * k + 1];
+                for (int k = 0; k < W; ++k) {
+                    e[k] = __fsub_rn(vec_elem<BF16>(raw[u], k), K);
+                    q[k] = e[k] * e[k];
                 }
-            acc_s += e[0];
-            acc_q += q[0];
-        } else {
-            const float v = __fsub_rn(load_elem<BF16>(p, 0), K);
-            acc_s += v;
-            acc_q += v * v;
+#pragma unroll
+                for (int w = W; w > 1; w >>= 1)
+#pragma unroll
+                    for (int k = 0; k < w / 2; ++k) {
+                        e[k] = e[2 * k] + e[2 * k + 1];
+                        q[k] = q[2 * k] + q[2 * k + 1];
+                    }
+                acc_s += e[0];
+                acc_q += q[0];
+            } else {
+                const float d = __fsub_rn(sc[u], K);
+                acc_s += d;
+                acc_q += d * d;
+            }
         }
     }
-    double ds = acc_s, dq = acc_q;
-    block_sum2(ds, dq);
-    if (threadIdx.x == 0) a.partial[static_cast<int64_t>(c) * a.S + s] = make_double2(ds, dq);
+    FF fs{acc_s, 0.0f}, fq{acc_q, 0.0f};
+    block_sum2_ff(fs, fq);
+    if (threadIdx.x == 0)
+        a.partial[static_cast<int64_t>(c) * a.S + s] = make_float2(__fadd_rn(fs.hi, fs.lo), __fadd_rn(fq.hi, fq.lo));
 }
 
+// CTA of 32 warps = 32 channels.  Warp w adds channel (32·blockIdx + w)'s S
+// partials in float-float (lane l takes slices l, l+32, ..., then a fixed
+// shuffle tree); warp 0 then finalises the 32 channels in fp64, one channel
+// per lane, so each fp64 instruction serves 32 channels.
+constexpr int kMergeThreads = 1024;
+
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads) bn_merge_kernel(const __grid_constant__ BnParams a) {
-    const int c = blockIdx.x * kThreads + threadIdx.x;
+__global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_constant__ BnParams a) {
+    __shared__ FF sums[2][32];
+    const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int c = blockIdx.x * 32 + w;
     pdl_enter();
-    if (c >= a.C) return;
-    double S = 0.0, Q = 0.0;
-    for (int s = 0; s < a.S; ++s) {
-        const double2 v = a.partial[static_cast<int64_t>(c) * a.S + s];
-        S += v.x;
-        Q += v.y;
+    FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
+    if (c < a.C) {
+        const float2* p = a.partial + static_cast<int64_t>(c) * a.S;
+        int s0 = lane;
+        for (; s0 + 96 < a.S; s0 += 128) {           // four independent loads in flight
+            const float2 v0 = p[s0], v1 = p[s0 + 32], v2 = p[s0 + 64], v3 = p[s0 + 96];
+            S = ff_add(ff_add(S, FF{v0.x, 0.0f}), ff_add(FF{v1.x, 0.0f}, ff_add(FF{v2.x, 0.0f}, FF{v3.x, 0.0f})));
+            Q = ff_add(ff_add(Q, FF{v0.y, 0.0f}), ff_add(FF{v1.y, 0.0f}, ff_add(FF{v2.y, 0.0f}, FF{v3.y, 0.0f})));
+        }
+        for (; s0 < a.S; s0 += 32) {
+            const float2 v = p[s0];
+            S = ff_add(S, FF{v.x, 0.0f});
+            Q = ff_add(Q, FF{v.y, 0.0f});
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        S = ff_add(S, ff_shfl_down(S, o));
+        Q = ff_add(Q, ff_shfl_down(Q, o));
+    }
+    if (lane == 0) {
+        sums[0][w] = S;
+        sums[1][w] = Q;
+    }
+    __syncthreads();
+    if (w != 0) return;
+    const int cc = blockIdx.x * 32 + lane;
+    if (cc >= a.C) return;
+    const double Sd = static_cast<double>(sums[0][lane].hi) + static_cast<double>(sums[0][lane].lo);
+    const double Qd = static_cast<double>(sums[1][lane].hi) + static_cast<double>(sums[1][lane].lo);
     const double M = static_cast<double>(a.n) * a.batch * a.HW;
-    const double K = static_cast<double>(load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW));
-    const double ms = S / M;
+    const double K = static_cast<double>(load_elem<BF16>(a.x[0], static_cast<int64_t>(cc) * a.HW));
+    const double ms = Sd / M;
     const double mean = K + ms;
-    const double var = Q / M - ms * ms;
+    const double var = Qd / M - ms * ms;
     const double invstd = 1.0 / sqrt(var + static_cast<double>(a.eps));
-    const double g = a.gamma ? static_cast<double>(a.gamma[c]) : 1.0;
-    const double b = a.beta ? static_cast<double>(a.beta[c]) : 0.0;
+    const double g = a.gamma ? static_cast<double>(a.gamma[cc]) : 1.0;
+    const double b = a.beta ? static_cast<double>(a.beta[cc]) : 0.0;
     const float m_hi = static_cast<float>(mean);
-    a.mean_out[c] = m_hi;
-    a.invstd_out[c] = static_cast<float>(invstd);
-    a.coef[c] = make_float4(m_hi, static_cast<float>(mean - static_cast<double>(m_hi)),
-                            static_cast<float>(invstd * g), static_cast<float>(b));
+    a.mean_out[cc] = m_hi;
+    a.invstd_out[cc] = static_cast<float>(invstd);
+    a.coef[cc] = make_float4(m_hi, static_cast<float>(mean - static_cast<double>(m_hi)),
+                             static_cast<float>(invstd * g), static_cast<float>(b));
 }
 
 // ((x − m_hi) − m_lo)·scale + β with k = (m_hi, m_lo, scale, β)
@@ -165,8 +473,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return l | (h << 16);
 }
 
-// CVEC: H*W is a multiple of 8, so the 8 elements of one access share a channel.
-template <bool BF16_IN, bool BF16_OUT, bool CVEC, bool NC>
+__device__ __forceinline__ uint32_t channel_of(uint32_t e, const BnParams& a) {
+    const uint32_t pl = fdiv(e, a.div_hw);
+    return pl - fdiv(pl, a.div_c) * static_cast<uint32_t>(a.C);
+}
+
+// CMODE: 0 = H*W a multiple of 8 (one channel per 8-element vector);
+//        1 = H*W >= 8 (at most one channel boundary inside a vector);
+//        2 = H*W < 8 (channel per element).
+template <bool BF16_IN, bool BF16_OUT, int CMODE, bool NC>
 __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constant__ BnParams a) {
     const int r = blockIdx.y;
     const char* x = static_cast<const char*>(a.x[r]);
@@ -177,66 +492,134 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
     const uint32_t stride = gridDim.x * kThreads;
     const uint32_t gtid = blockIdx.x * kThreads + threadIdx.x;
     pdl_enter();
-    for (uint32_t v = gtid; v < nvec; v += stride) {
-        const uint32_t e0 = v * 8;
-        float xv[8];
-        if constexpr (BF16_IN) {
-            const uint4 raw = ld16<NC>(x + static_cast<int64_t>(e0) * ISZ);
+    for (uint32_t v0 = gtid; v0 < nvec; v0 += 4 * stride) {
+        // issue the loads of 4 vectors before any arithmetic
+        uint4 raw[4][2];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) xv[k] = vec_elem<true>(raw, k);
-        } else {
-            const uint4 r0 = ld16<NC>(x + static_cast<int64_t>(e0) * ISZ);
-            const uint4 r1 = ld16<NC>(x + static_cast<int64_t>(e0) * ISZ + 16);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                xv[k] = vec_elem<false>(r0, k);
-                xv[4 + k] = vec_elem<false>(r1, k);
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t v = v0 + u * stride;
+            if (v < nvec) {
+                raw[u][0] = ld16<NC>(x + static_cast<int64_t>(v) * 8 * ISZ);
+                if constexpr (!BF16_IN) raw[u][1] = ld16<NC>(x + static_cast<int64_t>(v) * 8 * ISZ + 16);
             }
         }
-        float yv[8];
-        if constexpr (CVEC) {
-            const uint32_t pl = fdiv(e0, a.div_hw);
-            const uint32_t c = pl - fdiv(pl, a.div_c) * static_cast<uint32_t>(a.C);
-            const float4 k4 = __ldg(a.coef + c);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) yv[k] = normalize(xv[k], k4);
-        } else {
+        for (int u = 0; u < 4; ++u) {
+            const uint32_t v = v0 + u * stride;
+            if (v >= nvec) continue;
+            const uint32_t e0 = v * 8;
+            float xv[8];
+            if constexpr (BF16_IN) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t pl = fdiv(e0 + k, a.div_hw);
-                const uint32_t c = pl - fdiv(pl, a.div_c) * static_cast<uint32_t>(a.C);
-                yv[k] = normalize(xv[k], __ldg(a.coef + c));
+                for (int k = 0; k < 8; ++k) xv[k] = vec_elem<true>(raw[u][0], k);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    xv[k] = vec_elem<false>(raw[u][0], k);
+                    xv[4 + k] = vec_elem<false>(raw[u][1], k);
+                }
             }
-        }
-        if constexpr (BF16_OUT) {
-            st16(y + static_cast<int64_t>(e0) * OSZ,
-                 make_uint4(pack_bf16x2(yv[0], yv[1]), pack_bf16x2(yv[2], yv[3]), pack_bf16x2(yv[4], yv[5]),
-                            pack_bf16x2(yv[6], yv[7])));
-        } else {
-            st16(y + static_cast<int64_t>(e0) * OSZ, f4_bits(yv[0], yv[1], yv[2], yv[3]));
-            st16(y + static_cast<int64_t>(e0) * OSZ + 16, f4_bits(yv[4], yv[5], yv[6], yv[7]));
+            float yv[8];
+            if constexpr (CMODE == 0) {
+                const float4 k4 = __ldg(a.coef + channel_of(e0, a));
+#pragma unroll
+                for (int k = 0; k < 8; ++k) yv[k] = normalize(xv[k], k4);
+            } else if constexpr (CMODE == 1) {
+                const uint32_t pl = fdiv(e0, a.div_hw);
+                const uint32_t cross = static_cast<uint32_t>(a.HW) - (e0 - pl * static_cast<uint32_t>(a.HW));
+                const uint32_t c0 = pl - fdiv(pl, a.div_c) * static_cast<uint32_t>(a.C);
+                const float4 k0 = __ldg(a.coef + c0);
+                const float4 k1 = cross < 8 ? __ldg(a.coef + (c0 + 1 == static_cast<uint32_t>(a.C) ? 0 : c0 + 1)) : k0;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) yv[k] = normalize(xv[k], static_cast<uint32_t>(k) < cross ? k0 : k1);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) yv[k] = normalize(xv[k], __ldg(a.coef + channel_of(e0 + k, a)));
+            }
+            if constexpr (BF16_OUT) {
+                st16(y + static_cast<int64_t>(e0) * OSZ,
+                     make_uint4(pack_bf16x2(yv[0], yv[1]), pack_bf16x2(yv[2], yv[3]), pack_bf16x2(yv[4], yv[5]),
+                                pack_bf16x2(yv[6], yv[7])));
+            } else {
+                st16(y + static_cast<int64_t>(e0) * OSZ, f4_bits(yv[0], yv[1], yv[2], yv[3]));
+                st16(y + static_cast<int64_t>(e0) * OSZ + 16, f4_bits(yv[4], yv[5], yv[6], yv[7]));
+            }
         }
     }
     // tail: E % 8 elements
     const uint32_t t0 = nvec * 8;
     if (gtid < E - t0) {
         const uint32_t e = t0 + gtid;
-        const float xe = load_elem<BF16_IN>(x, e);
-        const uint32_t pl = fdiv(e, a.div_hw);
-        const uint32_t c = pl - fdiv(pl, a.div_c) * static_cast<uint32_t>(a.C);
-        const float ye = normalize(xe, a.coef[c]);
+        const float ye = normalize(load_elem<BF16_IN>(x, e), a.coef[channel_of(e, a)]);
         if constexpr (BF16_OUT) reinterpret_cast<__nv_bfloat16*>(y)[e] = __float2bfloat16_rn(ye);
         else reinterpret_cast<float*>(y)[e] = ye;
     }
 }
 
-// slices per channel for the stats grid
-int stats_slices(int32_t n, int32_t batch, int32_t C) {
-    const int P = n * batch;
-    int S = (kTargetCtas + C - 1) / C;
+// ---------------------------------------------------------------- launch planning (host)
+
+enum StatsKind { kPlaneVec, kPlaneScalar, kSegment, kStaged };
+
+struct StatsPlan {
+    StatsKind kind;
+    int G, S, R, slot_bytes;
+};
+
+int pow2_floor(int v) {
+    int p = 1;
+    while (p * 2 <= v) p *= 2;
+    return p;
+}
+
+// Channels per group of the group kernel: the largest power of two <= 256
+// with G*H*W <= kRunElems (at least 1), and no larger than C allows.
+int group_channels(int C, int HW) {
+    int G = 1;
+    while (G < kThreads && static_cast<int64_t>(2 * G) * HW <= kRunElems) G *= 2;
+    const int cap = pow2_floor(C);
+    return G < cap ? G : cap;
+}
+
+int slices_for(int n_groups, int P, int C) {
+    int64_t S = (kTargetCtas + n_groups - 1) / n_groups;
     if (S > P) S = P;
+    const int64_t cap = kMaxPartials / C;
+    if (S > cap) S = cap;
     if (S < 1) S = 1;
-    return S;
+    return static_cast<int>(S);
+}
+
+int slot_bytes_for(int G, int HW, int esz) {
+    return static_cast<int>((static_cast<int64_t>(G) * HW * esz + 14 + 15) / 16 * 16);
+}
+
+// Aligned planes: plane kernel with 16-byte loads.  Unaligned planes at
+// least one vector long: segment kernel.  Planes shorter than a vector:
+// staged group kernel.  Unaligned planes too long to fit a group's run in
+// the shared buffer: plane kernel with element loads.
+StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
+    StatsPlan sp{};
+    const int P = n * batch;
+    const int W = 16 / esz;
+    const int G = group_channels(C, HW);
+    const int slot = slot_bytes_for(G, HW, esz);
+    const bool fits = slot <= kStageBytes;
+    if (HW % W == 0) sp.kind = kPlaneVec;
+    else if (!fits) sp.kind = kPlaneScalar;
+    else sp.kind = HW >= W ? kSegment : kStaged;
+    if (sp.kind == kSegment || sp.kind == kStaged) {
+        sp.G = G;
+        sp.slot_bytes = slot;
+        sp.R = kStageBytes / slot;
+        if (sp.kind == kSegment && sp.R > kThreads / G) sp.R = kThreads / G;   // one (run, channel) pair per thread
+        sp.S = slices_for((C + G - 1) / G, P, C);
+    } else {
+        sp.G = 1;
+        sp.slot_bytes = 0;
+        sp.R = 0;
+        sp.S = slices_for(C, P, C);
+    }
+    return sp;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -250,14 +633,28 @@ bool valid_sizes(int32_t n, int32_t batch, int32_t C, int32_t H, int32_t W) {
            static_cast<int64_t>(n) * batch * hw < (int64_t(1) << 31);
 }
 
-template <bool BF16_IN, bool BF16_OUT>
-int launch_apply(const BnParams& p, bool cvec, bool nc, dim3 grid, cudaStream_t s) {
-    if (cvec) {
-        if (nc) return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, true, true>, grid, kThreads, s, p);
-        return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, true, false>, grid, kThreads, s, p);
+// Partials needed by any plan of these sizes (fp32 or bf16 input).
+int64_t max_partials(int32_t n, int32_t batch, int32_t C, int32_t HW) {
+    int64_t m = 0;
+    for (int esz : {2, 4}) {
+        const StatsPlan sp = plan_stats(n, batch, C, HW, esz);
+        const int64_t v = static_cast<int64_t>(C) * sp.S;
+        if (v > m) m = v;
     }
-    if (nc) return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, false, true>, grid, kThreads, s, p);
-    return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, false, false>, grid, kThreads, s, p);
+    return m;
+}
+
+template <bool BF16_IN, bool BF16_OUT, int CMODE>
+int launch_apply_mode(const BnParams& p, bool nc, dim3 grid, cudaStream_t s) {
+    if (nc) return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, CMODE, true>, grid, kThreads, s, p);
+    return launch_pdl(bn_apply_kernel<BF16_IN, BF16_OUT, CMODE, false>, grid, kThreads, s, p);
+}
+
+template <bool BF16_IN, bool BF16_OUT>
+int launch_apply(const BnParams& p, int cmode, bool nc, dim3 grid, cudaStream_t s) {
+    if (cmode == 0) return launch_apply_mode<BF16_IN, BF16_OUT, 0>(p, nc, grid, s);
+    if (cmode == 1) return launch_apply_mode<BF16_IN, BF16_OUT, 1>(p, nc, grid, s);
+    return launch_apply_mode<BF16_IN, BF16_OUT, 2>(p, nc, grid, s);
 }
 
 }  // namespace
@@ -267,8 +664,8 @@ using namespace ddp;
 
 extern "C" size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int32_t H, int32_t W) {
     if (!valid_sizes(n_replicas, batch, C, H, W)) return 0;
-    const int S = stats_slices(n_replicas, batch, C);
-    return align_up(static_cast<size_t>(C) * S * sizeof(double2), 16) + static_cast<size_t>(C) * sizeof(float4);
+    const int64_t parts = max_partials(n_replicas, batch, C, H * W);
+    return align_up(static_cast<size_t>(parts) * sizeof(float2), 16) + static_cast<size_t>(C) * sizeof(float4);
 }
 
 extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtype,
@@ -306,6 +703,10 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
             return DDP_ERR_INVALID_ARG;
     }
 
+    const bool bf16_in = in_dtype == DDP_BF16;
+    const int esz = bf16_in ? 2 : 4;
+    const StatsPlan sp = plan_stats(n_replicas, batch, C, H * W, esz);
+
     BnParams p{};
     for (int r = 0; r < n_replicas; ++r) {
         p.x[r] = x[r];
@@ -319,32 +720,44 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     p.batch = batch;
     p.C = C;
     p.HW = H * W;
-    p.S = stats_slices(n_replicas, batch, C);
+    p.S = sp.S;
+    p.G = sp.G;
+    p.R = sp.R;
+    p.slot_bytes = sp.slot_bytes;
     p.eps = eps;
     char* ws = static_cast<char*>(workspace);
-    p.partial = reinterpret_cast<double2*>(ws);
-    ws += align_up(static_cast<size_t>(C) * p.S * sizeof(double2), 16);
+    p.partial = reinterpret_cast<float2*>(ws);
+    ws += align_up(static_cast<size_t>(C) * p.S * sizeof(float2), 16);
     p.coef = reinterpret_cast<float4*>(ws);
-
-    const bool bf16_in = in_dtype == DDP_BF16;
-    const int wvec = bf16_in ? 8 : 4;
-    const bool vec = (p.HW % wvec) == 0;
-    p.div_unit = make_fastdiv(static_cast<uint32_t>(vec ? p.HW / wvec : p.HW));
     p.div_batch = make_fastdiv(static_cast<uint32_t>(batch));
     p.div_hw = make_fastdiv(static_cast<uint32_t>(p.HW));
     p.div_c = make_fastdiv(static_cast<uint32_t>(C));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const dim3 sgrid(static_cast<unsigned>(C), static_cast<unsigned>(p.S));
     int st;
-    if (bf16_in) st = vec ? launch_pdl(bn_stats_kernel<true, true>, sgrid, kThreads, s, p)
-                          : launch_pdl(bn_stats_kernel<true, false>, sgrid, kThreads, s, p);
-    else st = vec ? launch_pdl(bn_stats_kernel<false, true>, sgrid, kThreads, s, p)
-                  : launch_pdl(bn_stats_kernel<false, false>, sgrid, kThreads, s, p);
+    if (sp.kind == kSegment || sp.kind == kStaged) {
+        p.div_unit = make_fastdiv(static_cast<uint32_t>(sp.slot_bytes / 16));
+        const dim3 grid(static_cast<unsigned>((C + sp.G - 1) / sp.G), static_cast<unsigned>(sp.S));
+        if (sp.kind == kSegment)
+            st = bf16_in ? launch_pdl(bn_stats_segment_kernel<true>, grid, kThreads, s, p)
+                         : launch_pdl(bn_stats_segment_kernel<false>, grid, kThreads, s, p);
+        else
+            st = bf16_in ? launch_pdl(bn_stats_group_kernel<true>, grid, kThreads, s, p)
+                         : launch_pdl(bn_stats_group_kernel<false>, grid, kThreads, s, p);
+    } else {
+        const int wv = 16 / esz;
+        const bool vec = (p.HW % wv) == 0;
+        p.div_unit = make_fastdiv(static_cast<uint32_t>(vec ? p.HW / wv : p.HW));
+        const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(sp.S));
+        if (bf16_in) st = vec ? launch_pdl(bn_stats_plane_kernel<true, true>, grid, kThreads, s, p)
+                              : launch_pdl(bn_stats_plane_kernel<true, false>, grid, kThreads, s, p);
+        else st = vec ? launch_pdl(bn_stats_plane_kernel<false, true>, grid, kThreads, s, p)
+                      : launch_pdl(bn_stats_plane_kernel<false, false>, grid, kThreads, s, p);
+    }
     if (st != DDP_OK) return st;
-    const dim3 mgrid(static_cast<unsigned>((C + kThreads - 1) / kThreads));
-    st = bf16_in ? launch_pdl(bn_merge_kernel<true>, mgrid, kThreads, s, p)
-                 : launch_pdl(bn_merge_kernel<false>, mgrid, kThreads, s, p);
+    const dim3 mgrid(static_cast<unsigned>((C + 31) / 32));
+    st = bf16_in ? launch_pdl(bn_merge_kernel<true>, mgrid, kMergeThreads, s, p)
+                 : launch_pdl(bn_merge_kernel<false>, mgrid, kMergeThreads, s, p);
     if (st != DDP_OK) return st;
 
     DeviceInfo d;
@@ -356,11 +769,11 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     if (gx > cap) gx = cap;
     if (gx < 1) gx = 1;
     const dim3 agrid(static_cast<unsigned>(gx), static_cast<unsigned>(n_replicas));
-    const bool cvec = (p.HW % 8) == 0;
+    const int cmode = (p.HW % 8) == 0 ? 0 : (p.HW >= 8 ? 1 : 2);
     const bool nc = !in_place_any;
     const bool bf16_out = out_dtype == DDP_BF16;
-    if (bf16_in) return bf16_out ? launch_apply<true, true>(p, cvec, nc, agrid, s) : launch_apply<true, false>(p, cvec, nc, agrid, s);
-    return bf16_out ? launch_apply<false, true>(p, cvec, nc, agrid, s) : launch_apply<false, false>(p, cvec, nc, agrid, s);
+    if (bf16_in) return bf16_out ? launch_apply<true, true>(p, cmode, nc, agrid, s) : launch_apply<true, false>(p, cmode, nc, agrid, s);
+    return bf16_out ? launch_apply<false, true>(p, cmode, nc, agrid, s) : launch_apply<false, false>(p, cmode, nc, agrid, s);
 }
 
 // ---------------------------------------------------------------- variant without a caller workspace

@@ -193,8 +193,11 @@ size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int3
  *     S = Σ_r Σ x_r[:,c],  Q = Σ_r Σ x_r[:,c]²,  M = N·batch·H·W
  *     mean = S/M,  var = Q/M − mean²  (biased),  invstd = 1/sqrt(var + eps)
  *     y_r = (x_r − mean)·invstd·γ + β
- * Partial sums are fp32 over at most a few hundred elements, combined and
- * merged in fp64; the apply runs in fp32.
+ * Sums are shifted by each channel's first element (so Q/M − mean² does
+ * not cancel when |mean| >> std); threads accumulate a few hundred
+ * elements in fp32, each CTA combines its threads in fp64 and stores one
+ * fp32 partial per channel, and the partials are merged in fp64; the apply
+ * runs in fp32.
  *
  *   x            host array of n_replicas device pointers, each
  *                [batch, C, H, W] NCHW contiguous, in_dtype elements
@@ -230,7 +233,7 @@ int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtyp
  *   Arguments, results and errors are those of syncbn_merge_apply, without
  *   workspace/workspace_bytes.  Sizes whose syncbn_workspace_bytes(...)
  *   exceeds the fixed array are rejected with DDP_ERR_CAPACITY (every shape
- *   with C <= 32768 fits; C <= 2048 needs at most 96 KiB).
+ *   with C <= 43690 fits; C <= 2048 needs at most 544 KiB).
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress, with that device current) and caches it;
  *   make that first call before any stream capture.

@@ -85,7 +85,7 @@ def test_noalloc_rejects_oversize():
     f.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                   ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
-    C = 32769                                   # needs 32*C bytes > the 1 MiB array
+    C = 43691                                   # needs 24*C bytes > the 1 MiB array
     assert g.syncbn_workspace_bytes(2, 1, C, 1, 1) > g.syncbn_noalloc_max_workspace_bytes()
     x = [torch.zeros((1, C, 1, 1), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
     y = [torch.zeros_like(t) for t in x]
