@@ -14,7 +14,8 @@
 //      The kernel depends on the plane (H*W contiguous elements of one
 //      sample and channel):
 //        plane kernel — H*W a multiple of the 16-byte vector (56x56, 28x28):
-//          CTA (c, s) streams its planes with 16-byte loads.
+//          CTA (c, s) streams its planes with 16-byte loads, a warp at a
+//          time over 64-vector chunks of one plane.
 //        segment kernel — unaligned planes at least one vector long (7x7,
 //          14x14, 3x3): a CTA owns G consecutive channels (G*H*W about 2K
 //          elements) and a slice of the samples; for one sample those G
@@ -24,6 +25,7 @@
 //          one thread per (sample, channel) then adds its channel's segments.
 //        staged group kernel — planes shorter than a vector (1x1, 2x2):
 //          runs are copied to shared memory and reduced per channel there.
+//        element kernel — unaligned planes too long to stage (111x111).
 //      Every kernel reads a run's ragged end element by element, so no
 //      access leaves the replica buffer.
 //      Threads accumulate at most a few hundred elements in fp32 (vectors
@@ -219,15 +221,20 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
 // neighbouring groups, which are masked out).  Phase A: each thread turns
 // one vector into (Σd, Σd²) of its first channel and of the next one and
 // stores them in shared memory.  Phase B: thread (run j, channel cl, part k)
-// adds up the segments of channel cl's vectors.  A run's last vector is read
-// element by element where it would extend past the run, so no access
-// leaves the replica buffer.
+// adds up the segments of channel cl's vectors.  Interior vectors take a
+// mask-free path; only a run's first and last vectors are masked, and the
+// last one is read element by element where it would extend past the run,
+// so no access leaves the replica buffer.
+constexpr int kMaxRuns = 128;
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) bn_stats_segment_kernel(const __grid_constant__ BnParams a) {
     constexpr int ESZ = BF16 ? 2 : 4;
     constexpr int W = 16 / ESZ;
     __shared__ float4 seg[kStageBytes / 16];
-    __shared__ float Ks[kThreads];
+    __shared__ float Ks[kThreads + 1];
+    __shared__ const char* rbase[kMaxRuns];
+    __shared__ int32_t rpre[kMaxRuns];
     __shared__ float red[2][kThreads];
     const int c0 = blockIdx.x * a.G, s = blockIdx.y;
     const int Gc = min(a.G, a.C - c0);
@@ -236,73 +243,82 @@ __global__ void __launch_bounds__(kThreads) bn_stats_segment_kernel(const __grid
     const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
     const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
     const uint32_t vslot = static_cast<uint32_t>(a.slot_bytes / 16);   // vectors per run (upper bound)
-    const uint32_t run_elems = static_cast<uint32_t>(Gc) * HW;
+    const int32_t run_elems = Gc * HW;
     // phase-B role: pair (j, cl) and part k of Tk
     const int Tk = kThreads / (a.R * a.G);
     const int pair = threadIdx.x / Tk, k = threadIdx.x - pair * Tk;
     const int jb = pair / a.G, cl = pair - jb * a.G;
     pdl_enter();
     if (threadIdx.x < Gc) Ks[threadIdx.x] = load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + threadIdx.x) * HW);
-    __syncthreads();
+    if (threadIdx.x == 0) Ks[Gc] = 0.0f;      // read only for elements past the group, which are masked
 
     float acc_s = 0.0f, acc_q = 0.0f;
     for (int t0 = p0; t0 < p1; t0 += a.R) {
         const int nr = min(a.R, p1 - t0);
+        if (threadIdx.x < nr) {                       // per-run base (aligned down) and misalignment
+            const uint32_t pl = static_cast<uint32_t>(t0 + threadIdx.x);
+            const uint32_t r = fdiv(pl, a.div_batch);
+            const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
+            const uint64_t first = (static_cast<uint64_t>(b) * a.C + c0) * HW;
+            const uint32_t pre = static_cast<uint32_t>(first % W);
+            rbase[threadIdx.x] = static_cast<const char*>(a.x[r]) + (first - pre) * ESZ;
+            rpre[threadIdx.x] = static_cast<int32_t>(pre);
+        }
+        __syncthreads();
         // phase A
         const uint32_t total = static_cast<uint32_t>(nr) * vslot;
         for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
             const uint32_t j = fdiv(t, a.div_unit);
             const uint32_t v = t - j * vslot;
-            const uint32_t pl = static_cast<uint32_t>(t0) + j;
-            const uint32_t r = fdiv(pl, a.div_batch);
-            const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
-            const uint64_t first = (static_cast<uint64_t>(b) * a.C + c0) * HW;          // run's first element
-            const uint32_t pre = static_cast<uint32_t>(first % W);                      // elements before it in its vector
-            const int32_t e_start = static_cast<int32_t>(v * W) - static_cast<int32_t>(pre);
-            if (e_start >= static_cast<int32_t>(run_elems)) continue;
-            const char* base = static_cast<const char*>(a.x[r]) + (first - pre) * ESZ + 16ull * v;
-            float xe[W];
-            if (e_start + W <= static_cast<int32_t>(run_elems)) {     // the whole vector lies before the run's end
-                const uint4 raw = ld16<true>(base);
-#pragma unroll
-                for (int q = 0; q < W; ++q) xe[q] = vec_elem<BF16>(raw, q);
-            } else {
-#pragma unroll
-                for (int q = 0; q < W; ++q)
-                    xe[q] = (e_start + q < static_cast<int32_t>(run_elems)) ? load_elem<BF16>(base, q) : 0.0f;
-            }
+            const int32_t e_start = static_cast<int32_t>(v * W) - rpre[j];
+            if (e_start >= run_elems) continue;
+            const char* ptr = rbase[j] + 16ull * v;
             const uint32_t e_first = e_start > 0 ? static_cast<uint32_t>(e_start) : 0u;
-            const uint32_t ca = fdiv(e_first, a.div_hw);           // channel (in group) of the first valid element
-            const int32_t eb = static_cast<int32_t>((ca + 1) * HW); // first element of the next channel
-            const float Ka = Ks[ca];
-            const float Kb = (ca + 1 < static_cast<uint32_t>(Gc)) ? Ks[ca + 1] : 0.0f;
-            float sl = 0.0f, ql = 0.0f, sh = 0.0f, qh = 0.0f;
+            const uint32_t ca = fdiv(e_first, a.div_hw);                  // channel (in group) of the first element
+            const int32_t kb = static_cast<int32_t>((ca + 1) * HW) - e_start;   // elements before the next channel
+            const float Ka = Ks[ca], Kb = Ks[ca + 1];
+            float s_all = 0.0f, q_all = 0.0f, s_hi = 0.0f, q_hi = 0.0f;
+            if (e_start >= 0 && e_start + W <= run_elems) {              // interior vector: no masks
+                const uint4 raw = ld16<true>(ptr);
 #pragma unroll
-            for (int q = 0; q < W; ++q) {
-                const int32_t e = e_start + q;
-                const bool valid = e >= 0 && e < static_cast<int32_t>(run_elems);
-                const bool hi = e >= eb;
-                const float d = valid ? __fsub_rn(xe[q], hi ? Kb : Ka) : 0.0f;
-                if (hi) {
-                    sh += d;
-                    qh += d * d;
+                for (int q = 0; q < W; ++q) {
+                    const bool hi = q >= kb;
+                    const float d = __fsub_rn(vec_elem<BF16>(raw, q), hi ? Kb : Ka);
+                    const float dh = hi ? d : 0.0f;
+                    s_all += d;
+                    q_all = fmaf(d, d, q_all);
+                    s_hi += dh;
+                    q_hi = fmaf(dh, dh, q_hi);
+                }
+            } else {                                                      // first or last vector of the run
+                float xe[W];
+                if (e_start + W <= run_elems) {
+                    const uint4 raw = ld16<true>(ptr);
+#pragma unroll
+                    for (int q = 0; q < W; ++q) xe[q] = vec_elem<BF16>(raw, q);
                 } else {
-                    sl += d;
-                    ql += d * d;
+#pragma unroll
+                    for (int q = 0; q < W; ++q) xe[q] = (e_start + q < run_elems) ? load_elem<BF16>(ptr, q) : 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < W; ++q) {
+                    const int32_t e = e_start + q;
+                    const bool valid = e >= 0 && e < run_elems;
+                    const bool hi = q >= kb;
+                    const float d = valid ? __fsub_rn(xe[q], hi ? Kb : Ka) : 0.0f;
+                    const float dh = hi ? d : 0.0f;
+                    s_all += d;
+                    q_all = fmaf(d, d, q_all);
+                    s_hi += dh;
+                    q_hi = fmaf(dh, dh, q_hi);
                 }
             }
-            seg[j * vslot + v] = make_float4(sl, ql, sh, qh);
+            seg[j * vslot + v] = make_float4(__fsub_rn(s_all, s_hi), __fsub_rn(q_all, q_hi), s_hi, q_hi);
         }
         __syncthreads();
         // phase B
         if (jb < nr && cl < Gc) {
-            const uint64_t first = [&] {
-                const uint32_t pl = static_cast<uint32_t>(t0 + jb);
-                const uint32_t r = fdiv(pl, a.div_batch);
-                const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
-                return (static_cast<uint64_t>(b) * a.C + c0) * HW;
-            }();
-            const uint32_t pre = static_cast<uint32_t>(first % W);
+            const uint32_t pre = static_cast<uint32_t>(rpre[jb]);
             const uint32_t lo = pre + static_cast<uint32_t>(cl) * HW;       // element position in the vector grid
             const uint32_t hi = lo + HW - 1;
             for (uint32_t v = lo / W + k; v <= hi / W; v += Tk) {
@@ -325,9 +341,9 @@ __global__ void __launch_bounds__(kThreads) bn_stats_segment_kernel(const __grid
     __syncthreads();
     if (threadIdx.x < Gc) {
         FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
-        for (int j = 0; j < a.R; ++j)
+        for (int jj = 0; jj < a.R; ++jj)
             for (int q = 0; q < Tk; ++q) {
-                const int t = (j * a.G + threadIdx.x) * Tk + q;
+                const int t = (jj * a.G + threadIdx.x) * Tk + q;
                 S = ff_add(S, FF{red[0][t], 0.0f});
                 Q = ff_add(Q, FF{red[1][t], 0.0f});
             }
@@ -336,51 +352,59 @@ __global__ void __launch_bounds__(kThreads) bn_stats_segment_kernel(const __grid
     }
 }
 
-// Plane kernel, grid (C, S).  VEC: H*W is a multiple of the 16-byte vector
-// width (16-byte loads); otherwise single-element loads (only for planes too
-// large to stage and not vector aligned).
-template <bool BF16, bool VEC>
+// Plane kernel, grid (C, S), for H*W a multiple of the 16-byte vector width
+// W: CTA (c, s) reduces channel c over its slice of planes.  A warp owns a
+// chunk of 64 consecutive vectors of one plane (lane l reads vectors l and
+// l + 32 of the chunk: coalesced), so the plane and address arithmetic is
+// done once per chunk; each warp handles two chunks per iteration, four
+// 16-byte loads in flight per lane.
+constexpr int kChunkVecs = 64;
+
+template <bool BF16>
 __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_constant__ BnParams a) {
-    constexpr int W = VEC ? (BF16 ? 8 : 4) : 1;    // elements per access
+    constexpr int W = BF16 ? 8 : 4;    // elements per 16-byte access
     constexpr int ESZ = BF16 ? 2 : 4;
+    constexpr int kWarps = kThreads / 32;
     const int c = blockIdx.x, s = blockIdx.y;
+    const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     const int P = a.n * a.batch;
     const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
     const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
-    const uint32_t units = static_cast<uint32_t>(a.HW / W);     // accesses per plane
-    const uint32_t total = static_cast<uint32_t>(p1 - p0) * units;
+    const uint32_t units = static_cast<uint32_t>(a.HW / W);                     // vectors per plane
+    const uint32_t cpp = (units + kChunkVecs - 1) / kChunkVecs;                  // chunks per plane
+    const uint32_t total = static_cast<uint32_t>(p1 - p0) * cpp;
     pdl_enter();
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
     float acc_s = 0.0f, acc_q = 0.0f;
-    // 4 independent accesses per thread per iteration keep enough bytes in flight
-    for (uint32_t t0 = threadIdx.x; t0 < total; t0 += 4 * kThreads) {
-        uint4 raw[4];
-        float sc[4];
+    for (uint32_t ch0 = warp; ch0 < total; ch0 += 2 * kWarps) {
+        uint4 raw[2][2];
+        bool ok[2][2];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const uint32_t t = t0 + u * kThreads;
-            raw[u] = make_uint4(0, 0, 0, 0);
-            sc[u] = 0.0f;
-            if (t < total) {
-                const uint32_t pl_off = fdiv(t, a.div_unit);
-                const uint32_t uu = t - pl_off * units;
-                const uint32_t pl = static_cast<uint32_t>(p0) + pl_off;
-                const uint32_t r = fdiv(pl, a.div_batch);
-                const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
-                const int64_t elem = (static_cast<int64_t>(b) * a.C + c) * a.HW + static_cast<int64_t>(uu) * W;
-                const char* ptr = static_cast<const char*>(a.x[r]) + elem * ESZ;
-                if constexpr (VEC) raw[u] = ld16<true>(ptr);
-                else sc[u] = load_elem<BF16>(ptr, 0);
+        for (int i = 0; i < 2; ++i) {
+            const uint32_t ch = ch0 + i * kWarps;                               // warp-uniform
+            const uint32_t pl_off = fdiv(ch, a.div_unit);
+            const uint32_t cc = ch - pl_off * cpp;
+            const uint32_t pl = static_cast<uint32_t>(p0) + pl_off;
+            const uint32_t r = fdiv(pl, a.div_batch);
+            const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
+            const char* base = static_cast<const char*>(a.x[ch < total ? r : 0]) +
+                               (static_cast<int64_t>(b) * a.C + c) * a.HW * ESZ;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint32_t v = cc * kChunkVecs + u * 32 + lane;
+                ok[i][u] = ch < total && v < units;
+                raw[i][u] = ok[i][u] ? ld16<true>(base + static_cast<int64_t>(v) * 16) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (t0 + u * kThreads >= total) continue;
-            if constexpr (VEC) {
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (!ok[i][u]) continue;
                 float e[W], q[W];
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
-                    e[k] = __fsub_rn(vec_elem<BF16>(raw[u], k), K);
+                    e[k] = __fsub_rn(vec_elem<BF16>(raw[i][u], k), K);
                     q[k] = e[k] * e[k];
                 }
 #pragma unroll
@@ -392,11 +416,33 @@ __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_c
                     }
                 acc_s += e[0];
                 acc_q += q[0];
-            } else {
-                const float d = __fsub_rn(sc[u], K);
-                acc_s += d;
-                acc_q += d * d;
             }
+    }
+    FF fs{acc_s, 0.0f}, fq{acc_q, 0.0f};
+    block_sum2_ff(fs, fq);
+    if (threadIdx.x == 0)
+        a.partial[static_cast<int64_t>(c) * a.S + s] = make_float2(__fadd_rn(fs.hi, fs.lo), __fadd_rn(fq.hi, fq.lo));
+}
+
+// Element kernel, grid (C, S): planes that are neither vector aligned nor
+// small enough to stage (e.g. 111x111); single-element loads.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) bn_stats_element_kernel(const __grid_constant__ BnParams a) {
+    const int c = blockIdx.x, s = blockIdx.y;
+    const int P = a.n * a.batch;
+    const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
+    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
+    pdl_enter();
+    const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);
+    float acc_s = 0.0f, acc_q = 0.0f;
+    for (int pl = p0; pl < p1; ++pl) {
+        const int r = pl / a.batch, b = pl - r * a.batch;
+        const void* base = static_cast<const char*>(a.x[r]) +
+                           (static_cast<int64_t>(b) * a.C + c) * a.HW * (BF16 ? 2 : 4);
+        for (int e = threadIdx.x; e < a.HW; e += kThreads) {
+            const float d = __fsub_rn(load_elem<BF16>(base, e), K);
+            acc_s += d;
+            acc_q += d * d;
         }
     }
     FF fs{acc_s, 0.0f}, fq{acc_q, 0.0f};
@@ -612,6 +658,7 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
         sp.slot_bytes = slot;
         sp.R = kStageBytes / slot;
         if (sp.kind == kSegment && sp.R > kThreads / G) sp.R = kThreads / G;   // one (run, channel) pair per thread
+        if (sp.kind == kSegment && sp.R > kMaxRuns) sp.R = kMaxRuns;
         sp.S = slices_for((C + G - 1) / G, P, C);
     } else {
         sp.G = 1;
@@ -746,13 +793,16 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
                          : launch_pdl(bn_stats_group_kernel<false>, grid, kThreads, s, p);
     } else {
         const int wv = 16 / esz;
-        const bool vec = (p.HW % wv) == 0;
-        p.div_unit = make_fastdiv(static_cast<uint32_t>(vec ? p.HW / wv : p.HW));
         const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(sp.S));
-        if (bf16_in) st = vec ? launch_pdl(bn_stats_plane_kernel<true, true>, grid, kThreads, s, p)
-                              : launch_pdl(bn_stats_plane_kernel<true, false>, grid, kThreads, s, p);
-        else st = vec ? launch_pdl(bn_stats_plane_kernel<false, true>, grid, kThreads, s, p)
-                      : launch_pdl(bn_stats_plane_kernel<false, false>, grid, kThreads, s, p);
+        if (sp.kind == kPlaneVec) {
+            const uint32_t units = static_cast<uint32_t>(p.HW / wv);
+            p.div_unit = make_fastdiv((units + kChunkVecs - 1) / kChunkVecs);
+            st = bf16_in ? launch_pdl(bn_stats_plane_kernel<true>, grid, kThreads, s, p)
+                         : launch_pdl(bn_stats_plane_kernel<false>, grid, kThreads, s, p);
+        } else {
+            st = bf16_in ? launch_pdl(bn_stats_element_kernel<true>, grid, kThreads, s, p)
+                         : launch_pdl(bn_stats_element_kernel<false>, grid, kThreads, s, p);
+        }
     }
     if (st != DDP_OK) return st;
     const dim3 mgrid(static_cast<unsigned>((C + 31) / 32));
