@@ -68,6 +68,24 @@ def dist_env():
     return world, rank, local
 
 
+def dist_max(value: float, world: int, device=None) -> float:
+    """The largest of every rank's `value` (all ranks get it).  The tensor
+    lives on `device`: a CUDA device for NCCL, the CPU for gloo."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_rate(world: int, bytes_per_rank_step: float, steps: int, max_elapsed_ms: float) -> float:
+    """Whole-job GB/s: every rank moved bytes_per_rank_step per step; the
+    job took as long as its slowest rank."""
+    return world * bytes_per_rank_step * steps / (max_elapsed_ms * 1e-3) / 1e9
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -341,11 +359,8 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     clock_rows = sampler.stop() if rank == 0 else []
     local_ms = t_start.elapsed_time(t_end)
-    elapsed = torch.tensor([local_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(elapsed, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(elapsed.item())
-    value = world * step_bytes * K / (elapsed_ms * 1e-3) / 1e9
+    elapsed_ms = dist_max(local_ms, world, dev)
+    value = weak_scaling_rate(world, step_bytes, K, elapsed_ms)
 
     # The timed region runs nothing but the averaging kernel (K x 5 launches
     # back to back), so its average launch duration is the region time over
@@ -394,10 +409,7 @@ def run_ours(args, world, rank, local):
             e2e_step()
         e1.record()
     torch.cuda.synchronize()
-    e2e_ms = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
-    e2e_value = world * step_bytes * args.e2e_steps / (float(e2e_ms.item()) * 1e-3) / 1e9
+    e2e_value = weak_scaling_rate(world, step_bytes, args.e2e_steps, dist_max(e0.elapsed_time(e1), world, dev))
 
     rows = None
     if rank == 0 and world == 1 and not args.no_rows:

@@ -15,7 +15,8 @@
 // encryptions the thread writes -1 and counts the index in a status word
 // instead of looping on.  The kernel is integer-ALU bound (~4 rounds x
 // ~3.3 walks x 2 64-bit multiplies per index); the 8-byte output per index
-// is its only memory traffic.
+// is its only memory traffic.  Threads stream through several output slots
+// so that lanes of a warp stay busy although walk lengths differ.
 #include <cstdint>
 
 #include "common.cuh"
@@ -62,36 +63,50 @@ __device__ __forceinline__ uint64_t encrypt(uint64_t x, const SamplerParams& a) 
     return (L << a.h) | R;
 }
 
+// Position -> unshuffled index for output slot i.
+__device__ __forceinline__ uint64_t base_index(int64_t i, const SamplerParams& a) {
+    int64_t r, s;
+    if (a.rank >= 0) {
+        r = a.rank;
+        s = i;
+    } else {
+        r = i / a.ns;
+        s = i - r * a.ns;
+    }
+    const uint64_t pos = static_cast<uint64_t>(r) + static_cast<uint64_t>(s) * static_cast<uint64_t>(a.N);
+    return pos < a.n ? pos : pos % a.n;       // padding repeats the head
+}
+
+// Each thread owns output slots gtid, gtid + T, gtid + 2T, ... (T = grid
+// threads, about 8 slots per thread).  Cycle-walk lengths are geometric, so
+// instead of idling until the slowest lane of the warp has finished one
+// index, a thread starts its next slot as soon as one is done: every loop
+// iteration is exactly one encryption for every lane.
 __global__ void __launch_bounds__(kThreads) sampler_kernel(const __grid_constant__ SamplerParams a) {
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < a.count; i += stride) {
-        int64_t r, s;
-        if (a.rank >= 0) {
-            r = a.rank;
-            s = i;
-        } else {
-            r = i / a.ns;
-            s = i - r * a.ns;
-        }
-        const uint64_t pos = static_cast<uint64_t>(r) + static_cast<uint64_t>(s) * static_cast<uint64_t>(a.N);
-        const uint64_t j = pos < a.n ? pos : pos % a.n;       // padding repeats the head
-        int64_t v = static_cast<int64_t>(j);
-        if (a.shuffle && a.n > 1) {
-            uint64_t y = encrypt(j, a);
-            int steps = 1;
-            while (y >= a.n) {
-                if (steps >= kWalkCap) break;
-                y = encrypt(y, a);
-                ++steps;
-            }
-            if (y >= a.n) {
-                v = -1;
+    const int64_t T = static_cast<int64_t>(gridDim.x) * kThreads;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    if (!(a.shuffle && a.n > 1)) {
+        for (; i < a.count; i += T) a.out[i] = static_cast<int64_t>(base_index(i, a));
+        return;
+    }
+    if (i >= a.count) return;
+    uint64_t y = base_index(i, a);
+    int steps = 0;                             // encryptions applied to y
+    while (true) {
+        if (steps > 0 && (y < a.n || steps >= kWalkCap)) {
+            if (y < a.n) {
+                a.out[i] = static_cast<int64_t>(y);
+            } else {                           // walk bound reached: never observed
+                a.out[i] = -1;
                 if (a.status) atomicAdd(a.status, 1);
-            } else {
-                v = static_cast<int64_t>(y);
             }
+            i += T;
+            if (i >= a.count) break;
+            y = base_index(i, a);
+            steps = 0;
         }
-        a.out[i] = v;
+        y = encrypt(y, a);
+        ++steps;
     }
 }
 
@@ -152,8 +167,9 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     p.shuffle = shuffle;
 
     int grid = 0;
+    constexpr int64_t kSlotsPerThread = 8;
     const int st = one_wave_grid(reinterpret_cast<const void*>(sampler_kernel), kThreads,
-                                 (count + kThreads - 1) / kThreads, &grid);
+                                 (count + kSlotsPerThread * kThreads - 1) / (kSlotsPerThread * kThreads), &grid);
     if (st != DDP_OK) return st;
     // plain launch: the status word's memset just before must complete first
     sampler_kernel<<<grid, kThreads, 0, s>>>(p);
