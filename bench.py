@@ -44,6 +44,7 @@ CAP_BYTES = 25 * MiB
 METRIC = "bucket allreduce-mean GB/s (HBM bytes moved) & % of HBM roofline, 1×GB300"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 10 ** 6
+SAMPLER_LANE_INSTR_PER_INDEX = 423.0   # ncu, 1,281,167 items over 8 ranks (profiles/sampler_imagenet.md)
 
 
 def parse_args():
@@ -535,9 +536,16 @@ def bench_rows(g, torch, dev, peak, peak_kind):
     n, N = workloads.SAMPLER_N_ITEMS, workloads.SAMPLER_REPLICAS
     out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
     ms = _time_launches(torch, lambda: g.dist_sampler_indices(n, N, -1, 0, 1, True, False, out), 100, side)
+    # ALU roofline: lane-instruction issue peak (152 SMs x 4 schedulers x 32 lanes x 2.07 GHz) over the
+    # lane-instructions one index needs on this workload (ncu, profiles/sampler_imagenet.md)
+    lane_issue_peak = 152 * 4 * 32 * 2.07e9
+    idx_per_s = out.numel() / (ms * 1e-3)
+    peak_idx = lane_issue_peak / SAMPLER_LANE_INSTR_PER_INDEX
     rows["sampler_imagenet"] = {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
-                                "Mindex_per_s": out.numel() / ms / 1e3, "bytes": out.numel() * 8,
-                                "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu", "launches": 1}
+                                "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
+                                "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
+                                "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
+                                "launches": 1}
     rows["_peak"] = {"hbm_gbs": peak, "source": peak_kind}
     return rows
 
