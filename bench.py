@@ -515,6 +515,38 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                                     "frac": nbytes / ms / 1e6 / peak, "launches": 2}
     del reps, theta, buf, outb
 
+    # gradient accumulation (no_sync micro-step) and the clipped final step, GPT-2 small, fp32 accumulators
+    plan4 = g.ddp_plan_buckets(num, 4, 0, g.PLAN_DEEP_FIRST, first)
+    total4 = plan4["total_elems"]
+    acc = [torch.zeros(total4, device=dev) for _ in range(N_REPLICAS)]
+    micro = [workloads.device_normal((total4,), 0.0, 0.01, workloads.seed_for(3, r) + 50, device=dev,
+                                     dtype=torch.bfloat16) for r in range(N_REPLICAS)]
+    ms = _time_launches(torch, lambda: g.ddp_bucket_accumulate(micro, acc), 20, side)
+    nbytes = (2 + 8) * N_REPLICAS * total4
+    rows["accumulate_gpt2_small"] = {"workload": "GPT-2 small, 8 replicas, bf16 micro-step gradient added into "
+                                                 "fp32 accumulators (no_sync)", "ms": ms, "bytes": nbytes,
+                                     "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 1}
+    del micro
+    gavg = torch.empty(total4, device=dev)
+    theta = workloads.device_normal((total4,), 0.0, 0.02, workloads.seed_for(3, 99), device=dev)
+    buf = torch.zeros(total4, device=dev)
+    ws = torch.empty(g.ddp_norm_workspace_bytes(len(plan4["buckets"])), dtype=torch.uint8, device=dev)
+    coef = torch.empty(1, device=dev)
+
+    def clipped_step():
+        for b, (off, n, _, _) in enumerate(plan4["buckets"]):
+            g.ddp_bucket_allreduce_mean_norm([x[off:off + n] for x in acc], gavg[off:off + n], ws, b)
+        g.ddp_grad_norm_finalize(ws, len(plan4["buckets"]), 1.0, None, coef, None)
+        for off, n, _, _ in plan4["buckets"]:
+            g.ddp_bucket_sgd(gavg[off:off + n], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, grad_scale=coef)
+    ms = _time_launches(torch, clipped_step, 20, side)
+    nbytes = sum(((N_REPLICAS + 1) * 4 + 20) * b[1] for b in plan4["buckets"])
+    rows["clipped_step_gpt2_small"] = {"workload": "GPT-2 small, 8 fp32 accumulated replicas: average with norm "
+                                                   "side output, clip to 1.0, SGD momentum 0.9 wd 1e-4",
+                                       "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
+                                       "frac": nbytes / ms / 1e6 / peak, "launches": 5}
+    del acc, gavg, theta, buf
+
     # SyncBN, 4 shapes
     for C, H, W in workloads.SYNCBN_SHAPES:
         B = workloads.SYNCBN_BATCH

@@ -267,3 +267,61 @@ def syncbn_noalloc_max_workspace_bytes() -> int:
 
 
 __all__ += ["syncbn_merge_apply_noalloc", "syncbn_noalloc_max_workspace_bytes"]
+
+
+# ---------------------------------------------------------------- accumulation, norm / clipping, non-finite
+
+NORM_SLOTS = 2048
+_lib.ddp_bucket_accumulate.argtypes = [_P, _P, _c.c_int32, _c.c_int32, _c.c_int64, _P]
+_lib.ddp_bucket_accumulate.restype = _c.c_int
+_lib.ddp_norm_workspace_bytes.argtypes = [_c.c_int32]
+_lib.ddp_norm_workspace_bytes.restype = _c.c_size_t
+_lib.ddp_bucket_allreduce_mean_norm.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int64, _P, _P, _c.c_int32, _P]
+_lib.ddp_bucket_allreduce_mean_norm.restype = _c.c_int
+_lib.ddp_grad_norm_finalize.argtypes = [_P, _c.c_int32, _c.c_float, _P, _P, _P, _P]
+_lib.ddp_grad_norm_finalize.restype = _c.c_int
+_lib.ddp_bucket_sgd.argtypes = [_P, _P, _P, _c.c_int64, _c.c_float, _c.c_float, _c.c_float, _P, _P]
+_lib.ddp_bucket_sgd.restype = _c.c_int
+
+
+def ddp_bucket_accumulate(micro, acc, numel=None, stream=None) -> None:
+    """acc[r] += micro[r] for every replica r (micro fp32 or bf16, acc fp32)."""
+    if len(micro) != len(acc) or not 1 <= len(micro) <= MAX_REPLICAS:
+        raise ValueError("need 1..16 replicas and one accumulator per replica")
+    n = int(numel if numel is not None else micro[0].numel())
+    _check(_lib.ddp_bucket_accumulate(_ptr_array(micro), _ptr_array(acc), len(micro), _dtype_code(micro[0]), n,
+                                      _stream_ptr(stream)), "ddp_bucket_accumulate")
+
+
+def ddp_norm_workspace_bytes(n_buckets: int) -> int:
+    return int(_lib.ddp_norm_workspace_bytes(n_buckets))
+
+
+def ddp_bucket_allreduce_mean_norm(replicas, out, norm_ws, bucket_index: int, numel=None, stream=None) -> None:
+    """Rank-ordered average into out plus bucket bucket_index's Σout² and
+    non-finite flag in norm_ws (a uint8 device tensor)."""
+    if not 1 <= len(replicas) <= MAX_REPLICAS:
+        raise ValueError("need 1..16 replicas")
+    n = int(numel if numel is not None else replicas[0].numel())
+    _check(_lib.ddp_bucket_allreduce_mean_norm(_ptr_array(replicas), len(replicas), _dtype_code(replicas[0]), n,
+                                               _ptr(out), _ptr(norm_ws), bucket_index, _stream_ptr(stream)),
+           "ddp_bucket_allreduce_mean_norm")
+
+
+def ddp_grad_norm_finalize(norm_ws, n_buckets: int, max_norm: float, norm_out=None, clip_coef_out=None,
+                           nonfinite_out=None, stream=None) -> None:
+    """Global norm, clip factor and non-finite flag of the step, in device memory."""
+    _check(_lib.ddp_grad_norm_finalize(_ptr(norm_ws), n_buckets, max_norm, _ptr(norm_out), _ptr(clip_coef_out),
+                                       _ptr(nonfinite_out), _stream_ptr(stream)), "ddp_grad_norm_finalize")
+
+
+def ddp_bucket_sgd(grad, param, momentum_buf, lr: float, momentum: float, weight_decay: float, grad_scale=None,
+                   numel=None, stream=None) -> None:
+    """SGD on an averaged fp32 gradient, optionally multiplied by a device scalar first."""
+    n = int(numel if numel is not None else grad.numel())
+    _check(_lib.ddp_bucket_sgd(_ptr(grad), _ptr(param), _ptr(momentum_buf), n, lr, momentum, weight_decay,
+                               _ptr(grad_scale), _stream_ptr(stream)), "ddp_bucket_sgd")
+
+
+__all__ += ["ddp_bucket_accumulate", "ddp_norm_workspace_bytes", "ddp_bucket_allreduce_mean_norm",
+            "ddp_grad_norm_finalize", "ddp_bucket_sgd", "NORM_SLOTS"]

@@ -35,6 +35,8 @@ enum Order { kRank = 0, kTree = 1, kRing = 2 };
 struct MeanParams {
     RepPtrs rep;
     float* out;
+    float4* norm_slots;   // NORM: per-CTA (Σout² hi, lo, non-finite flag, 0), one per CTA
+    int32_t* norm_count;  // NORM: number of CTAs that wrote a slot
     int64_t numel;
     int64_t ring_base;  // ring chunk j has ring_base + (j < ring_rem) elements
     int64_t ring_rem;
@@ -82,7 +84,9 @@ __device__ float mean_one(const MeanParams& a, int64_t e) {
     return scale_by_n(acc, a.pow2, a.inv_n, n);
 }
 
-template <int NMAX, bool BF16, int ORDER, bool WB, bool NC>
+// NORM: also reduce Σ out² and "any out non-finite" over the CTA and store
+// them in the CTA's slot (side output for gradient clipping and the NaN check).
+template <int NMAX, bool BF16, int ORDER, bool WB, bool NC, bool NORM = false>
 __global__ void __launch_bounds__(kThreads) mean_kernel(const __grid_constant__ MeanParams a) {
     constexpr int VEC = BF16 ? 8 : 4;   // elements per 16-byte input vector
     constexpr int ESZ = BF16 ? 2 : 4;
@@ -90,6 +94,8 @@ __global__ void __launch_bounds__(kThreads) mean_kernel(const __grid_constant__ 
     const int64_t nvec = a.numel / VEC;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    float nsq = 0.0f;       // NORM: this thread's Σ out²
+    bool nonfinite = false; // NORM: this thread saw a NaN or infinity
     pdl_enter();
 
     for (int64_t v = gtid; v < nvec; v += stride) {
@@ -151,6 +157,13 @@ __global__ void __launch_bounds__(kThreads) mean_kernel(const __grid_constant__ 
                 res[k] = scale_by_n(acc, a.pow2, a.inv_n, n);
             }
         }
+        if constexpr (NORM) {
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                nsq = fmaf(res[k], res[k], nsq);
+                nonfinite |= (__float_as_uint(res[k]) & 0x7f800000u) == 0x7f800000u;
+            }
+        }
 #pragma unroll
         for (int q = 0; q < VEC / 4; ++q) {
             const uint4 o = f4_bits(res[4 * q], res[4 * q + 1], res[4 * q + 2], res[4 * q + 3]);
@@ -170,9 +183,22 @@ __global__ void __launch_bounds__(kThreads) mean_kernel(const __grid_constant__ 
         const int64_t e = tail0 + gtid;
         const float m = mean_one<BF16, ORDER>(a, e);
         a.out[e] = m;
+        if constexpr (NORM) {
+            nsq = fmaf(m, m, nsq);
+            nonfinite |= (__float_as_uint(m) & 0x7f800000u) == 0x7f800000u;
+        }
         if constexpr (WB) {
             for (int r = 0; r < n; ++r)
                 if (a.rep.p[r] != a.out) const_cast<float*>(static_cast<const float*>(a.rep.p[r]))[e] = m;
+        }
+    }
+    if constexpr (NORM) {
+        const bool any_nf = __syncthreads_or(nonfinite);
+        FF s{nsq, 0.0f}, unused{0.0f, 0.0f};
+        block_sum2_ff(s, unused);
+        if (threadIdx.x == 0) {
+            a.norm_slots[blockIdx.x] = make_float4(s.hi, s.lo, any_nf ? 1.0f : 0.0f, 0.0f);
+            if (blockIdx.x == 0) *a.norm_count = static_cast<int32_t>(gridDim.x);
         }
     }
 }
@@ -261,13 +287,15 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
 
 // ---------------------------------------------------------------- host side
 
-// One wave of CTAs for a bucket of nvec 16-byte vectors, then a PDL launch.
+// One wave of CTAs (at most max_grid) for a bucket of nvec 16-byte vectors,
+// then a PDL launch.
 template <typename Params>
-int launch_wave(void (*kernel)(Params), int64_t nvec, cudaStream_t s, const Params& p) {
+int launch_wave(void (*kernel)(Params), int64_t nvec, cudaStream_t s, const Params& p, int max_grid = 1 << 30) {
     int grid = 0;
     const int st = one_wave_grid(reinterpret_cast<const void*>(kernel), kThreads,
                                  (nvec + kThreads - 1) / kThreads, &grid);
     if (st != DDP_OK) return st;
+    if (grid > max_grid) grid = max_grid;
     return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), kThreads, s, p);
 }
 
@@ -415,4 +443,61 @@ extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_r
     const int64_t nvec = numel / (in_dtype == DDP_BF16 ? 8 : 4);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return in_dtype == DDP_BF16 ? dispatch_sgd<true>(p, nvec, s) : dispatch_sgd<false>(p, nvec, s);
+}
+
+
+// ---------------------------------------------------------------- average with a norm side output
+
+namespace ddp {
+namespace {
+
+template <bool BF16>
+int dispatch_mean_norm(const MeanParams& p, int64_t nvec, cudaStream_t s, bool aliased) {
+    if (p.n <= 4)
+        return aliased ? launch_wave(mean_kernel<4, BF16, kRank, false, false, true>, nvec, s, p, DDP_NORM_SLOTS)
+                       : launch_wave(mean_kernel<4, BF16, kRank, false, true, true>, nvec, s, p, DDP_NORM_SLOTS);
+    if (p.n <= 8)
+        return aliased ? launch_wave(mean_kernel<8, BF16, kRank, false, false, true>, nvec, s, p, DDP_NORM_SLOTS)
+                       : launch_wave(mean_kernel<8, BF16, kRank, false, true, true>, nvec, s, p, DDP_NORM_SLOTS);
+    return aliased ? launch_wave(mean_kernel<16, BF16, kRank, false, false, true>, nvec, s, p, DDP_NORM_SLOTS)
+                   : launch_wave(mean_kernel<16, BF16, kRank, false, true, true>, nvec, s, p, DDP_NORM_SLOTS);
+}
+
+}  // namespace
+}  // namespace ddp
+
+extern "C" int ddp_bucket_allreduce_mean_norm(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                                              int64_t numel, float* out, void* norm_ws, int32_t bucket_index,
+                                              void* stream) {
+    int st = check_replicas(replicas, n_replicas, in_dtype, numel);
+    if (st != DDP_OK) return st;
+    if (norm_ws == nullptr || bucket_index < 0 || (out == nullptr && numel > 0)) return DDP_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(norm_ws)) return DDP_ERR_ALIGNMENT;
+    const size_t esz = in_dtype == DDP_BF16 ? 2 : 4;
+    const size_t in_bytes = static_cast<size_t>(numel) * esz, out_bytes = static_cast<size_t>(numel) * 4;
+    char* slot = static_cast<char*>(norm_ws) + static_cast<size_t>(bucket_index) * kNormBucketBytes;
+    bool aliased = false;
+    for (int r = 0; r < n_replicas; ++r) {
+        if (static_cast<const void*>(out) == replicas[r] && in_dtype == DDP_F32) aliased = true;
+        else if (overlaps(out, out_bytes, replicas[r], in_bytes)) return DDP_ERR_INVALID_ARG;
+        if (overlaps(slot, kNormBucketBytes, replicas[r], in_bytes)) return DDP_ERR_INVALID_ARG;
+    }
+    if (overlaps(slot, kNormBucketBytes, out, out_bytes)) return DDP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (numel == 0) {      // an empty bucket contributes nothing: record zero CTAs
+        const cudaError_t e = cudaMemsetAsync(slot + kNormSlotBytes, 0, sizeof(int32_t), s);
+        return e == cudaSuccess ? DDP_OK : cuda_fail(e);
+    }
+    MeanParams p{};
+    for (int r = 0; r < n_replicas; ++r) p.rep.p[r] = replicas[r];
+    p.out = out;
+    p.numel = numel;
+    p.n = n_replicas;
+    p.pow2 = is_pow2(n_replicas);
+    p.inv_n = 1.0f / static_cast<float>(n_replicas);
+    p.norm_slots = reinterpret_cast<float4*>(slot);
+    p.norm_count = reinterpret_cast<int32_t*>(slot + kNormSlotBytes);
+    const int64_t nvec = numel / (in_dtype == DDP_BF16 ? 8 : 4);
+    return in_dtype == DDP_BF16 ? dispatch_mean_norm<true>(p, nvec, s, aliased)
+                                : dispatch_mean_norm<false>(p, nvec, s, aliased);
 }

@@ -11,6 +11,12 @@
 
 namespace ddp {
 
+// Norm workspace: per bucket DDP_NORM_SLOTS float4 slots (one per CTA of the
+// bucket's launch: Σout² as a float-float pair, a non-finite flag) followed by
+// the number of CTAs that wrote a slot, padded to 16 bytes.
+constexpr size_t kNormSlotBytes = static_cast<size_t>(DDP_NORM_SLOTS) * 16;
+constexpr size_t kNormBucketBytes = kNormSlotBytes + 16;
+
 // Record a CUDA error for ddp_last_cuda_error() and return DDP_ERR_CUDA.
 int cuda_fail(cudaError_t e);
 
@@ -19,10 +25,11 @@ int check_launch();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// [a, a+na) and [b, b+nb) share at least one byte.
+// [a, a+na) and [b, b+nb) share at least one byte (a NULL pointer is an
+// absent buffer and overlaps nothing).
 inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
     uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return na > 0 && nb > 0 && x < y + nb && y < x + na;
+    return a != nullptr && b != nullptr && na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
 struct DeviceInfo {

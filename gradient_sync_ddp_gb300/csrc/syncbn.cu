@@ -79,52 +79,6 @@ struct BnParams {
     float eps;
 };
 
-// Float-float arithmetic: a value is hi + lo, kept with fp32 operations only
-// (Knuth's TwoSum, then a renormalising Fast2Sum), about 48 significant bits.
-// GB300's FP64 pipe is narrow (one 32-lane fp64 instruction occupies it for
-// many cycles), so the reductions here avoid fp64 and use this instead; the
-// order of every reduction is fixed, so results are deterministic.
-struct FF {
-    float hi, lo;
-};
-
-__device__ __forceinline__ FF ff_add(FF a, FF b) {
-    const float s = __fadd_rn(a.hi, b.hi);
-    const float bb = __fsub_rn(s, a.hi);
-    const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
-    const float t = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
-    const float hi = __fadd_rn(s, t);
-    return FF{hi, __fsub_rn(t, __fsub_rn(hi, s))};
-}
-
-__device__ __forceinline__ FF ff_shfl_down(FF v, int o) {
-    return FF{__shfl_down_sync(0xffffffffu, v.hi, o), __shfl_down_sync(0xffffffffu, v.lo, o)};
-}
-
-// Sum of two per-thread values over the CTA in float-float, result in thread 0.
-__device__ __forceinline__ void block_sum2_ff(FF& a, FF& b) {
-    __shared__ FF sh[2][kThreads / 32];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        a = ff_add(a, ff_shfl_down(a, o));
-        b = ff_add(b, ff_shfl_down(b, o));
-    }
-    const int w = threadIdx.x / 32, l = threadIdx.x % 32;
-    if (l == 0) {
-        sh[0][w] = a;
-        sh[1][w] = b;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        a = sh[0][0];
-        b = sh[1][0];
-        for (int i = 1; i < kThreads / 32; ++i) {
-            a = ff_add(a, sh[0][i]);
-            b = ff_add(b, sh[1][i]);
-        }
-    }
-}
-
 template <bool BF16>
 __device__ __forceinline__ float shared_elem(const unsigned char* p, int e) {
     if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(p)[e]) << 16);

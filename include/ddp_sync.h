@@ -179,6 +179,78 @@ int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_replicas, in
                              float* grad_out, uint32_t flags, void* stream);
 
 /*
+ * ---- gradient accumulation, global norm with clipping, non-finite check ----
+ *
+ * [DDP] §5.2: with gradient accumulation, micro-steps run under no_sync (the
+ * gradient is only added into .grad locally, loss divided by the number of
+ * steps), the all-reduce runs once after the last micro-step, and
+ * clip_grad_norm_ is applied to the synced gradient before the optimizer
+ * step.  [TR24] §十一: a NaN-check graph (n_ncg) runs after the gradient
+ * syncs.  Flow on one GPU:
+ *   micro-steps:  ddp_bucket_accumulate (acc[r] += micro[r], every replica)
+ *   last step:    ddp_bucket_allreduce_mean_norm for each bucket (average +
+ *                 per-CTA Σg², non-finite flag), ddp_grad_norm_finalize
+ *                 (norm, clip factor, flag; all in device memory, no host
+ *                 sync), ddp_bucket_sgd for each bucket with the clip factor.
+ */
+
+/*
+ * ddp_bucket_accumulate — acc[r][i] = acc[r][i] + (float)micro[r][i] for every
+ * replica r (one fp32 rounding per element; bf16 micro gradients are widened
+ * exactly).
+ *   micro       host array of n_replicas device pointers, numel in_dtype each
+ *   acc         host array of n_replicas device pointers, numel float each,
+ *               updated in place; no acc buffer may overlap another buffer of
+ *               the call
+ */
+int ddp_bucket_accumulate(const void* const* micro, float* const* acc, int32_t n_replicas, int32_t in_dtype,
+                          int64_t numel, void* stream);
+
+#define DDP_NORM_SLOTS 2048
+
+/* Bytes of the norm workspace for n_buckets buckets (0 if n_buckets < 1). */
+size_t ddp_norm_workspace_bytes(int32_t n_buckets);
+
+/*
+ * ddp_bucket_allreduce_mean_norm — ddp_bucket_allreduce_mean in rank order
+ * (same bits in out), plus a side output for clipping: the bucket's Σ out[i]²
+ * (per-CTA partials, fp32 per thread, float-float per CTA) and whether any
+ * out[i] is NaN or infinite, stored in slot `bucket_index` of norm_ws.
+ *   norm_ws       device buffer of ddp_norm_workspace_bytes(n_buckets) bytes,
+ *                 16-byte aligned; each bucket of a step writes its own slot
+ *   bucket_index  0 .. n_buckets-1
+ * flags are not taken (rank order, no write-back).
+ */
+int ddp_bucket_allreduce_mean_norm(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                                   int64_t numel, float* out, void* norm_ws, int32_t bucket_index, void* stream);
+
+/*
+ * ddp_grad_norm_finalize — combine the slots of buckets 0..n_buckets-1 (all
+ * written in this step) into, in device memory:
+ *   norm_out       sqrt(Σ over every bucket of Σ out²)   (float)
+ *   clip_coef_out  min(1, max_norm / (norm + 1e-6)); 1 if max_norm <= 0
+ *                  (clip_grad_norm_'s factor)            (float)
+ *   nonfinite_out  1 if any averaged gradient element is NaN or infinite,
+ *                  else 0                                (int32)
+ * Any of the three outputs may be NULL.  One small kernel; no host sync.
+ */
+int ddp_grad_norm_finalize(const void* norm_ws, int32_t n_buckets, float max_norm, float* norm_out,
+                           float* clip_coef_out, int32_t* nonfinite_out, void* stream);
+
+/*
+ * ddp_bucket_sgd — the SGD step of ddp_bucket_allreduce_sgd applied to an
+ * already averaged gradient, optionally scaled first by a device scalar:
+ *     d = grad * (*grad_scale)        (if grad_scale != NULL; one rounding)
+ *     d = d + weight_decay*θ; b = momentum*buf + d; buf = b; θ = θ − lr*b
+ *   grad          device float[numel] (the averaged gradient), read only
+ *   param, momentum_buf, lr, momentum, weight_decay   as ddp_bucket_allreduce_sgd
+ *   grad_scale    device float or NULL, e.g. clip_coef_out of
+ *                 ddp_grad_norm_finalize
+ */
+int ddp_bucket_sgd(const float* grad, float* param, float* momentum_buf, int64_t numel, float lr,
+                   float momentum, float weight_decay, const float* grad_scale, void* stream);
+
+/*
  * syncbn_workspace_bytes — device workspace that syncbn_merge_apply needs
  * for these sizes (0 for invalid sizes).
  */

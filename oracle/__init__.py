@@ -11,17 +11,22 @@ from .ddp_oracle import (  # noqa: F401
     PLAN_CAP,
     PLAN_DEEP_FIRST,
     WALK_CAP,
+    accumulate,
+    any_nonfinite,
     bf16_bits_to_f32,
+    clip_coefficient,
     dist_sampler_indices,
     f64_to_bf16_rne,
     feistel_encrypt,
     grad_mean,
+    grad_global_norm,
     grad_mean_tree,
     keyed_perm,
     keyed_perm_all,
     plan_buckets,
     ring_allreduce_mean,
     sampler_num_samples,
+    sgd_from_grad,
     sgd_step,
     splitmix64_mix,
     splitmix64_stream,

@@ -444,3 +444,63 @@ def dist_sampler_indices(n: int, n_replicas: int, rank: int, seed: int, epoch: i
     if rank >= 0:
         return padded[rank:total:n_replicas].copy()
     return np.stack([padded[r:total:n_replicas] for r in range(n_replicas)]) if n_replicas else padded
+
+# ---------------------------------------------------------------------------
+# gradient accumulation, global norm / clipping, non-finite check
+# ([DDP] §5.2; [TR24] §十一 NaN-check graph)
+# ---------------------------------------------------------------------------
+
+
+def accumulate(acc: np.ndarray, micro: np.ndarray, dtype: str = "f32") -> np.ndarray:
+    """acc + micro in fp32: one micro-step of gradient accumulation under
+    no_sync ([DDP] §5.2: backward adds the new gradient into .grad; the
+    all-reduce runs only after the last micro-step).  dtype "f64" runs the
+    same addition in fp64 (used by the no_sync identity check)."""
+    acc_t = np.float64 if dtype == "f64" else np.float32
+    return np.ascontiguousarray(acc, dtype=acc_t) + _as_f32(micro, dtype)
+
+
+def grad_global_norm(grads) -> float:
+    """L2 norm of all averaged gradients together, in fp64: the quantity
+    clip_grad_norm_ computes after accumulation and the all-reduce
+    ([DDP] §5.2, point ③)."""
+    total = 0.0
+    for g in grads:
+        g64 = np.asarray(g, dtype=np.float64)
+        total += float(np.dot(g64, g64))
+    return math.sqrt(total)
+
+
+def clip_coefficient(norm: float, max_norm: float) -> float:
+    """The factor clip_grad_norm_ multiplies gradients by: max_norm divided by
+    (norm + 1e-6), never above 1.  max_norm <= 0 disables clipping (factor 1).
+    The pages only name clip_grad_norm_(..., 1.0); the formula is PyTorch's."""
+    if max_norm <= 0.0:
+        return 1.0
+    return min(1.0, max_norm / (norm + 1e-6))
+
+
+def any_nonfinite(grads) -> bool:
+    """True if any averaged gradient element is NaN or infinite (the role of
+    the NaN-check graph n_ncg in [TR24] §十一)."""
+    return any(not np.all(np.isfinite(np.asarray(g, dtype=np.float64))) for g in grads)
+
+
+def sgd_from_grad(g: np.ndarray, theta: np.ndarray, buf, lr: float, momentum: float, weight_decay: float,
+                  scale=None):
+    """The SGD step of sgd_step on an already averaged gradient, optionally
+    multiplied first by a clipping factor (one fp32 rounding):
+        d = g*scale (if scale is given); d = d + wd*θ; b = μ*buf + d; θ = θ − lr*b
+    Returns (theta_new, buf_new_or_None)."""
+    f = np.float32
+    d = np.ascontiguousarray(g, dtype=np.float32)
+    if scale is not None:
+        d = d * f(scale)
+    th = np.ascontiguousarray(theta, dtype=np.float32)
+    if weight_decay != 0.0:
+        d = d + f(weight_decay) * th
+    b_new = None
+    if momentum != 0.0:
+        b_new = f(momentum) * np.ascontiguousarray(buf, dtype=np.float32) + d
+        d = b_new
+    return th - f(lr) * d, b_new

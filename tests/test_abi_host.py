@@ -213,3 +213,44 @@ def test_sampler_host_logic(g):
     assert f(-1, 3, 0, 0, 0, 1, 0, FAKE, 100, ctypes.addressof(ns), None, None) == g.DDP_ERR_INVALID_ARG
     assert f(2, 3, 0, 0, 0, 1, 1, None, 0, ctypes.addressof(ns), None, None) == g.DDP_OK   # n < N, drop_last
     assert ns.value == 0
+
+
+def test_accum_clip_rejects(g):
+    lib = g.lib_handle()
+    two = _ptrs(FAKE, FAKE + 4096)
+    acc = _ptrs(FAKE + 8192, FAKE + 12288)
+    a = lib.ddp_bucket_accumulate
+    assert a(two, acc, 0, 0, 8, None) == g.DDP_ERR_INVALID_ARG
+    assert a(two, acc, 2, 3, 8, None) == g.DDP_ERR_INVALID_ARG
+    assert a(two, _ptrs(FAKE + 8192, FAKE + 8200), 2, 0, 8, None) == g.DDP_ERR_ALIGNMENT
+    assert a(two, _ptrs(FAKE, FAKE + 12288), 2, 0, 8, None) == g.DDP_ERR_INVALID_ARG      # acc on a micro
+    assert a(two, _ptrs(FAKE + 8192, FAKE + 8192), 2, 0, 8, None) == g.DDP_ERR_INVALID_ARG  # acc twice
+    assert a(two, acc, 2, 1, 0, None) == g.DDP_OK
+    assert g.ddp_norm_workspace_bytes(0) == 0
+    assert g.ddp_norm_workspace_bytes(3) == 3 * (2048 * 16 + 16)
+    m = lib.ddp_bucket_allreduce_mean_norm
+    assert m(two, 2, 0, 8, FAKE + 8192, None, 0, None) == g.DDP_ERR_INVALID_ARG
+    assert m(two, 2, 0, 8, FAKE + 8192, FAKE + 65536, -1, None) == g.DDP_ERR_INVALID_ARG
+    assert m(two, 2, 0, 8, FAKE + 8192, FAKE + 65544, 0, None) == g.DDP_ERR_ALIGNMENT
+    assert m(two, 2, 0, 8, FAKE + 8192, FAKE, 0, None) == g.DDP_ERR_INVALID_ARG           # workspace on a replica
+    f = lib.ddp_grad_norm_finalize
+    assert f(None, 1, 1.0, None, None, None, None) == g.DDP_ERR_INVALID_ARG
+    assert f(FAKE, 0, 1.0, None, None, None, None) == g.DDP_ERR_INVALID_ARG
+    assert f(FAKE, 1, float("nan"), None, None, None, None) == g.DDP_ERR_INVALID_ARG
+    assert f(FAKE, 1, 1.0, FAKE + 2, None, None, None) == g.DDP_ERR_ALIGNMENT
+    assert f(FAKE, 1, 1.0, FAKE + 16, None, None, None) == g.DDP_ERR_INVALID_ARG          # output inside ws
+    s = lib.ddp_bucket_sgd
+    G, P, B = FAKE, FAKE + 4096, FAKE + 8192
+    assert s(G, P, None, 8, 0.1, 0.9, 0.0, None, None) == g.DDP_ERR_INVALID_ARG          # needs the buffer
+    assert s(G, P, B, 8, 0.1, 0.0, 0.0, None, None) == g.DDP_ERR_INVALID_ARG             # buffer unused
+    assert s(G, G + 16, B, 8, 0.1, 0.9, 0.0, None, None) == g.DDP_ERR_INVALID_ARG        # θ overlaps grad
+    assert s(G, P + 4, B, 8, 0.1, 0.9, 0.0, None, None) == g.DDP_ERR_ALIGNMENT
+    assert s(G, P, B, 0, 0.1, 0.9, 0.0, None, None) == g.DDP_OK
+
+
+def test_absent_buffers_never_overlap(g):
+    """NULL optional outputs (no momentum buffer, no scale) are accepted."""
+    lib = g.lib_handle()
+    assert lib.ddp_bucket_sgd(FAKE, FAKE + 4096, None, 0, 0.1, 0.0, 0.0, None, None) == g.DDP_OK
+    two = _ptrs(FAKE, FAKE + 4096)
+    assert lib.ddp_bucket_allreduce_sgd(two, 2, 0, 0, FAKE + 8192, None, 0.1, 0.0, 0.0, None, 0, None) == g.DDP_OK

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
+import test_oracle_accum_clip as tac
 import test_oracle_mean as tm
 import test_oracle_orders as to
 import test_oracle_planner as tp
@@ -225,3 +226,33 @@ def _bn_variant(kind):
 @pytest.mark.parametrize("kind", ["unbiased", "eps_outside", "local_stats"])
 def test_syncbn_mutants_are_caught(kind):
     assert _trips([tb.check_syncbn_two_pass, tb.check_syncbn_vs_torch_batch_norm], _bn_variant(kind))
+
+
+def test_accumulate_mutants_are_caught():
+    def minus(acc, micro, dtype="f32"):
+        return oracle.accumulate(acc, -np.asarray(micro) if dtype != "bf16" else micro, dtype)
+
+    def first_only(acc, micro, dtype="f32"):
+        return np.asarray(acc, np.float64 if dtype == "f64" else np.float32) * 0 + oracle.ddp_oracle._as_f32(micro, dtype)
+
+    for bad in (minus, first_only):
+        assert _trips([lambda f: tac.check_no_sync_equivalence(f, oracle.grad_mean)], bad)
+
+
+@pytest.mark.parametrize("kind", ["no_sqrt", "no_clamp", "no_eps", "abs_sum"])
+def test_norm_clip_mutants_are_caught(kind):
+    def norm(grads):
+        if kind == "no_sqrt":
+            return oracle.grad_global_norm(grads) ** 2
+        if kind == "abs_sum":
+            return float(sum(np.abs(np.asarray(g, np.float64)).sum() for g in grads))
+        return oracle.grad_global_norm(grads)
+
+    def coef(n, m):
+        if kind == "no_clamp":
+            return m / (n + 1e-6) if m > 0 else 1.0
+        if kind == "no_eps":
+            return min(1.0, m / n) if m > 0 else 1.0
+        return oracle.clip_coefficient(n, m)
+
+    assert _trips([lambda _: tac.check_norm_and_clip(norm, coef)], None)
