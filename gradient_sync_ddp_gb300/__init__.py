@@ -325,3 +325,28 @@ def ddp_bucket_sgd(grad, param, momentum_buf, lr: float, momentum: float, weight
 
 __all__ += ["ddp_bucket_accumulate", "ddp_norm_workspace_bytes", "ddp_bucket_allreduce_mean_norm",
             "ddp_grad_norm_finalize", "ddp_bucket_sgd", "NORM_SLOTS"]
+
+
+# ---------------------------------------------------------------- BN running statistics
+
+_lib.bn_running_stats_update.argtypes = [_P, _P, _c.c_int64, _c.c_float, _P, _P, _c.c_int32, _P]
+_lib.bn_running_stats_update.restype = _c.c_int
+_lib.bn_fold_inference_params.argtypes = [_P, _P, _P, _P, _c.c_float, _c.c_int32, _P, _P, _P]
+_lib.bn_fold_inference_params.restype = _c.c_int
+
+
+def bn_running_stats_update(batch_mean, batch_var, count: int, momentum: float, running_mean, running_var,
+                            stream=None) -> None:
+    _check(_lib.bn_running_stats_update(_ptr(batch_mean), _ptr(batch_var), count, momentum, _ptr(running_mean),
+                                        _ptr(running_var), running_mean.numel(), _stream_ptr(stream)),
+           "bn_running_stats_update")
+
+
+def bn_fold_inference_params(running_mean, running_var, gamma, beta, eps: float, scale_out, bias_out,
+                             stream=None) -> None:
+    _check(_lib.bn_fold_inference_params(_ptr(running_mean), _ptr(running_var), _ptr(gamma), _ptr(beta), eps,
+                                         running_mean.numel(), _ptr(scale_out), _ptr(bias_out),
+                                         _stream_ptr(stream)), "bn_fold_inference_params")
+
+
+__all__ += ["bn_running_stats_update", "bn_fold_inference_params"]

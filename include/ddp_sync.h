@@ -325,6 +325,40 @@ int syncbn_merge_apply_noalloc(const void* const* x, int32_t n_replicas, int32_t
 size_t syncbn_noalloc_max_workspace_bytes(void);
 
 /*
+ * ---- BatchNorm running statistics ([TR24] §十二) ----
+ * STATS_COMM + UPDATE_STATS (mean all-reduce of every rank's running mean /
+ * var, then copy into the "previous" buffers) is ddp_bucket_allreduce_mean
+ * over the replicas' [mean | var] buffers with out = the previous-statistics
+ * buffer and DDP_FLAG_WRITE_BACK_ALL; the validation-metric mean
+ * (VAL_RESULT_COMM, [TR24] §十三) is the same call on the metric sums.  The
+ * two entries below are the per-channel steps around it.
+ */
+
+/*
+ * bn_running_stats_update — running statistics from one batch (PyTorch's
+ * rule; the pages do not give one):
+ *   running_mean = (1 − momentum)·running_mean + momentum·batch_mean
+ *   running_var  = (1 − momentum)·running_var  + momentum·batch_var·count/(count − 1)
+ * fp32, each operation rounded on its own; (1 − momentum) and
+ * count/(count − 1) are rounded to fp32 once on the host.
+ *   batch_mean, batch_var      device float[C] (biased batch variance)
+ *   count                      values per channel in the batch (>= 1)
+ *   momentum                   in [0, 1]
+ *   running_mean, running_var  device float[C], updated in place
+ */
+int bn_running_stats_update(const float* batch_mean, const float* batch_var, int64_t count, float momentum,
+                            float* running_mean, float* running_var, int32_t C, void* stream);
+
+/*
+ * bn_fold_inference_params — UPDATE_BN_INF_PARAMS: eq_scale = γ/sqrt(var + eps),
+ * eq_bias = β − mean·eq_scale (fp64 inside, fp32 out), so inference BN is
+ * y = x·eq_scale + eq_bias.  gamma / beta may be NULL (1 / 0).
+ */
+int bn_fold_inference_params(const float* running_mean, const float* running_var, const float* gamma,
+                             const float* beta, float eps, int32_t C, float* scale_out, float* bias_out,
+                             void* stream);
+
+/*
  * dist_sampler_num_samples — indices per rank ([DDP] §4.4):
  * floor(n/N) with drop_last, else ceil(n/N).  -1 on invalid input.
  */

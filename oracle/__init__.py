@@ -14,6 +14,8 @@ from .ddp_oracle import (  # noqa: F401
     accumulate,
     any_nonfinite,
     bf16_bits_to_f32,
+    bn_fold_inference,
+    bn_running_update,
     clip_coefficient,
     dist_sampler_indices,
     f64_to_bf16_rne,

@@ -504,3 +504,39 @@ def sgd_from_grad(g: np.ndarray, theta: np.ndarray, buf, lr: float, momentum: fl
         b_new = f(momentum) * np.ascontiguousarray(buf, dtype=np.float32) + d
         d = b_new
     return th - f(lr) * d, b_new
+
+# ---------------------------------------------------------------------------
+# BN running statistics and inference folding ([TR24] §十二)
+# ---------------------------------------------------------------------------
+
+
+def bn_running_update(running_mean, running_var, batch_mean, batch_var, count: int, momentum: float):
+    """One running-statistics update from a batch's mean and biased variance
+    over `count` values per channel.  [TR24] §十二 keeps per-rank running
+    statistics (B_NEXT_MEAN / B_NEXT_VAR) that are then mean-all-reduced; the
+    update rule itself is not on the pages — the reading is PyTorch's BN:
+        r_mean = (1 − m)·r_mean + m·batch_mean
+        r_var  = (1 − m)·r_var  + m·batch_var·count/(count − 1)
+    in fp32, each operation rounded on its own; (1 − m) and count/(count−1)
+    are computed in fp64 and rounded to fp32 once."""
+    f = np.float32
+    keep = f(1.0 - momentum)
+    mom = f(momentum)
+    corr = f(count / (count - 1)) if count > 1 else f(1.0)
+    rm = keep * np.asarray(running_mean, np.float32) + mom * np.asarray(batch_mean, np.float32)
+    unb = np.asarray(batch_var, np.float32) * corr
+    rv = keep * np.asarray(running_var, np.float32) + mom * unb
+    return rm, rv
+
+
+def bn_fold_inference(running_mean, running_var, gamma, beta, eps: float):
+    """UPDATE_BN_INF_PARAMS of [TR24] §十二: the per-channel scale and bias
+    that make BN at inference one multiply-add, y = x·eq_scale + eq_bias.
+    Reading (standard BN folding), in fp64:
+        eq_scale = γ / sqrt(running_var + eps),  eq_bias = β − running_mean·eq_scale"""
+    rm = np.asarray(running_mean, np.float64)
+    rv = np.asarray(running_var, np.float64)
+    g = np.ones_like(rm) if gamma is None else np.asarray(gamma, np.float64)
+    b = np.zeros_like(rm) if beta is None else np.asarray(beta, np.float64)
+    scale = g / np.sqrt(rv + eps)
+    return scale, b - rm * scale

@@ -254,3 +254,18 @@ def test_absent_buffers_never_overlap(g):
     assert lib.ddp_bucket_sgd(FAKE, FAKE + 4096, None, 0, 0.1, 0.0, 0.0, None, None) == g.DDP_OK
     two = _ptrs(FAKE, FAKE + 4096)
     assert lib.ddp_bucket_allreduce_sgd(two, 2, 0, 0, FAKE + 8192, None, 0.1, 0.0, 0.0, None, 0, None) == g.DDP_OK
+
+
+def test_bn_stats_rejects(g):
+    lib = g.lib_handle()
+    u = lib.bn_running_stats_update
+    A, B, C, D = FAKE, FAKE + 4096, FAKE + 8192, FAKE + 12288
+    assert u(A, B, 0, 0.1, C, D, 8, None) == g.DDP_ERR_INVALID_ARG       # count
+    assert u(A, B, 10, 1.5, C, D, 8, None) == g.DDP_ERR_INVALID_ARG      # momentum
+    assert u(A, B, 10, 0.1, C, C + 16, 8, None) == g.DDP_ERR_INVALID_ARG # running buffers overlap
+    assert u(A, B, 10, 0.1, C + 2, D, 8, None) == g.DDP_ERR_ALIGNMENT
+    assert u(A, B, 10, 0.1, C, D, 0, None) == g.DDP_OK
+    f = lib.bn_fold_inference_params
+    assert f(A, B, None, None, -1.0, 8, C, D, None) == g.DDP_ERR_INVALID_ARG
+    assert f(A, B, None, None, 1e-5, 8, A, D, None) == g.DDP_ERR_INVALID_ARG   # output on an input
+    assert f(A, B, None, None, 1e-5, 0, C, D, None) == g.DDP_OK

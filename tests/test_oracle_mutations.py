@@ -256,3 +256,26 @@ def test_norm_clip_mutants_are_caught(kind):
         return oracle.clip_coefficient(n, m)
 
     assert _trips([lambda _: tac.check_norm_and_clip(norm, coef)], None)
+
+
+def test_bn_stats_mutants_are_caught():
+    import test_oracle_bn_stats as tbs
+
+    def biased(rm, rv, bm, bv, count, m):
+        return oracle.bn_running_update(rm, rv, bm, bv, 2 ** 40, m)        # drops the count/(count-1) factor
+
+    def swapped(rm, rv, bm, bv, count, m):
+        return oracle.bn_running_update(rm, rv, bm, bv, count, 1.0 - m)    # momentum on the wrong side
+
+    for bad in (biased, swapped):
+        assert _trips([tbs.check_running_update], bad)
+
+    def no_eps(rm, rv, gamma, beta, eps):
+        return oracle.bn_fold_inference(rm, rv, gamma, beta, 0.0)
+
+    def plus_mean(rm, rv, gamma, beta, eps):
+        sc, bi = oracle.bn_fold_inference(rm, rv, gamma, beta, eps)
+        return sc, bi + 2 * np.asarray(rm) * sc                             # sign of the mean term
+
+    for bad in (no_eps, plus_mean):
+        assert _trips([tbs.check_fold], bad)
