@@ -502,6 +502,20 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                                           "SGD momentum 0.9 wd 1e-4", "ms": ms, "bytes": nbytes,
                               "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
 
+    # the same step also writing the bf16 compute copy of θ
+    low = torch.empty(total, dtype=torch.bfloat16, device=dev)
+
+    def sgd_cast_step():
+        for off, n, _, _ in plan["buckets"]:
+            g.ddp_bucket_allreduce_sgd_cast([x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n],
+                                            0.1, 0.9, 1e-4, low[off:off + n])
+    ms = _time_launches(torch, sgd_cast_step, 50, side)
+    nbytes = sum((2 * N_REPLICAS + 18) * b[1] for b in plan["buckets"])
+    rows["sgd_cast_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, SGD momentum 0.9 wd 1e-4 plus the "
+                                               "bf16 copy of θ", "ms": ms, "bytes": nbytes,
+                                   "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+    del low
+
     # bf16 -> fp32 average of the same buckets
     outb = torch.empty(total, device=dev)
 

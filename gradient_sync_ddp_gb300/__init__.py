@@ -280,7 +280,7 @@ _lib.ddp_bucket_allreduce_mean_norm.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c
 _lib.ddp_bucket_allreduce_mean_norm.restype = _c.c_int
 _lib.ddp_grad_norm_finalize.argtypes = [_P, _c.c_int32, _c.c_float, _P, _P, _P, _P]
 _lib.ddp_grad_norm_finalize.restype = _c.c_int
-_lib.ddp_bucket_sgd.argtypes = [_P, _P, _P, _c.c_int64, _c.c_float, _c.c_float, _c.c_float, _P, _P]
+_lib.ddp_bucket_sgd.argtypes = [_P, _P, _P, _c.c_int64, _c.c_float, _c.c_float, _c.c_float, _P, _P, _P]
 _lib.ddp_bucket_sgd.restype = _c.c_int
 
 
@@ -316,11 +316,12 @@ def ddp_grad_norm_finalize(norm_ws, n_buckets: int, max_norm: float, norm_out=No
 
 
 def ddp_bucket_sgd(grad, param, momentum_buf, lr: float, momentum: float, weight_decay: float, grad_scale=None,
-                   numel=None, stream=None) -> None:
-    """SGD on an averaged fp32 gradient, optionally multiplied by a device scalar first."""
+                   param_bf16=None, numel=None, stream=None) -> None:
+    """SGD on an averaged fp32 gradient, optionally multiplied by a device
+    scalar first; optionally also writes θ rounded to bf16."""
     n = int(numel if numel is not None else grad.numel())
     _check(_lib.ddp_bucket_sgd(_ptr(grad), _ptr(param), _ptr(momentum_buf), n, lr, momentum, weight_decay,
-                               _ptr(grad_scale), _stream_ptr(stream)), "ddp_bucket_sgd")
+                               _ptr(grad_scale), _ptr(param_bf16), _stream_ptr(stream)), "ddp_bucket_sgd")
 
 
 __all__ += ["ddp_bucket_accumulate", "ddp_norm_workspace_bytes", "ddp_bucket_allreduce_mean_norm",
@@ -350,3 +351,23 @@ def bn_fold_inference_params(running_mean, running_var, gamma, beta, eps: float,
 
 
 __all__ += ["bn_running_stats_update", "bn_fold_inference_params"]
+
+
+_lib.ddp_bucket_allreduce_sgd_cast.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int64, _P, _P, _c.c_float, _c.c_float,
+                                               _c.c_float, _P, _P, _P]
+_lib.ddp_bucket_allreduce_sgd_cast.restype = _c.c_int
+
+
+def ddp_bucket_allreduce_sgd_cast(replicas, param, momentum_buf, lr: float, momentum: float, weight_decay: float,
+                                  param_bf16, grad_out=None, numel=None, stream=None) -> None:
+    """ddp_bucket_allreduce_sgd that also writes the updated θ rounded to bf16 into param_bf16."""
+    if not 1 <= len(replicas) <= MAX_REPLICAS:
+        raise ValueError("need 1..16 replicas")
+    n = int(numel if numel is not None else replicas[0].numel())
+    _check(_lib.ddp_bucket_allreduce_sgd_cast(_ptr_array(replicas), len(replicas), _dtype_code(replicas[0]), n,
+                                              _ptr(param), _ptr(momentum_buf), lr, momentum, weight_decay,
+                                              _ptr(grad_out), _ptr(param_bf16), _stream_ptr(stream)),
+           "ddp_bucket_allreduce_sgd_cast")
+
+
+__all__ += ["ddp_bucket_allreduce_sgd_cast"]

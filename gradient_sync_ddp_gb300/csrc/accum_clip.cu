@@ -126,6 +126,7 @@ struct SgdGradParams {
     float* param;
     float* buf;
     const float* scale;
+    __nv_bfloat16* lowp;   // optional bf16 copy of the updated θ
     int64_t numel;
     float lr, mom, wd;
 };
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(kThreads) sgd_grad_kernel(const __grid_constan
             }
             st16(a.param + 4 * v, f4_bits(th[0], th[1], th[2], th[3]));
             if (has_mom) st16(a.buf + 4 * v, f4_bits(b[0], b[1], b[2], b[3]));
+            if (a.lowp != nullptr) st8(a.lowp + 4 * v, make_uint2(pack_bf16x2(th[0], th[1]), pack_bf16x2(th[2], th[3])));
         }
     }
     const int64_t tail0 = nvec * 4;
@@ -183,6 +185,7 @@ __global__ void __launch_bounds__(kThreads) sgd_grad_kernel(const __grid_constan
         sgd_from_grad(a, a.grad[e], sc, has_scale, th, b);
         a.param[e] = th;
         if (has_mom) a.buf[e] = b;
+        if (a.lowp != nullptr) a.lowp[e] = __float2bfloat16_rn(th);
     }
 }
 
@@ -254,19 +257,22 @@ extern "C" int ddp_grad_norm_finalize(const void* norm_ws, int32_t n_buckets, fl
 }
 
 extern "C" int ddp_bucket_sgd(const float* grad, float* param, float* momentum_buf, int64_t numel, float lr,
-                              float momentum, float weight_decay, const float* grad_scale, void* stream) {
+                              float momentum, float weight_decay, const float* grad_scale, void* param_bf16,
+                              void* stream) {
     if (numel < 0 || numel > INT64_MAX / 16) return DDP_ERR_INVALID_ARG;
     if (!(lr == lr) || !(momentum == momentum) || !(weight_decay == weight_decay)) return DDP_ERR_INVALID_ARG;
     const bool has_mom = momentum != 0.0f;
     if (!has_mom && momentum_buf != nullptr) return DDP_ERR_INVALID_ARG;
     if (numel > 0 && (grad == nullptr || param == nullptr || (has_mom && momentum_buf == nullptr)))
         return DDP_ERR_INVALID_ARG;
-    if (!aligned16(grad) || !aligned16(param) || !aligned16(momentum_buf) ||
+    if (!aligned16(grad) || !aligned16(param) || !aligned16(momentum_buf) || !aligned16(param_bf16) ||
         (reinterpret_cast<uintptr_t>(grad_scale) & 3u))
         return DDP_ERR_ALIGNMENT;
-    const size_t b = static_cast<size_t>(numel) * 4;
+    const size_t b = static_cast<size_t>(numel) * 4, hb = static_cast<size_t>(numel) * 2;
     if (overlaps(grad, b, param, b) || overlaps(grad, b, momentum_buf, b) || overlaps(param, b, momentum_buf, b) ||
-        overlaps(grad_scale, 4, param, b) || overlaps(grad_scale, 4, momentum_buf, b))
+        overlaps(grad_scale, 4, param, b) || overlaps(grad_scale, 4, momentum_buf, b) ||
+        overlaps(param_bf16, hb, grad, b) || overlaps(param_bf16, hb, param, b) ||
+        overlaps(param_bf16, hb, momentum_buf, b) || overlaps(param_bf16, hb, grad_scale, 4))
         return DDP_ERR_INVALID_ARG;
     if (numel == 0) return DDP_OK;
     SgdGradParams p{};
@@ -274,6 +280,7 @@ extern "C" int ddp_bucket_sgd(const float* grad, float* param, float* momentum_b
     p.param = param;
     p.buf = momentum_buf;
     p.scale = grad_scale;
+    p.lowp = static_cast<__nv_bfloat16*>(param_bf16);
     p.numel = numel;
     p.lr = lr;
     p.mom = momentum;

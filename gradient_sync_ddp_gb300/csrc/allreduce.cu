@@ -208,6 +208,7 @@ struct SgdParams {
     float* param;
     float* buf;
     float* gout;
+    __nv_bfloat16* lowp;   // optional bf16 copy of the updated θ
     int64_t numel;
     int32_t n;
     int32_t pow2;
@@ -261,6 +262,13 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
             b[k] = vec_elem<false>(bv[k / 4], k % 4);
             sgd_elem(a, g[k], th[k], b[k]);
         }
+        if (a.lowp != nullptr) {
+            if constexpr (VEC == 8)
+                st16(a.lowp + e0, make_uint4(pack_bf16x2(th[0], th[1]), pack_bf16x2(th[2], th[3]),
+                                             pack_bf16x2(th[4], th[5]), pack_bf16x2(th[6], th[7])));
+            else
+                st8(a.lowp + e0, make_uint2(pack_bf16x2(th[0], th[1]), pack_bf16x2(th[2], th[3])));
+        }
 #pragma unroll
         for (int q = 0; q < VEC / 4; ++q) {
             st16(a.param + e0 + 4 * q, f4_bits(th[4 * q], th[4 * q + 1], th[4 * q + 2], th[4 * q + 3]));
@@ -282,6 +290,7 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
         a.param[e] = th;
         if (has_mom) a.buf[e] = b;
         if (a.gout != nullptr) a.gout[e] = g;
+        if (a.lowp != nullptr) a.lowp[e] = __float2bfloat16_rn(th);
     }
 }
 
@@ -403,10 +412,9 @@ extern "C" int ddp_bucket_allreduce_mean(const void* const* replicas, int32_t n_
                                 : dispatch_mean<false>(p, nvec, s, order, wb, aliased);
 }
 
-extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
-                                        int64_t numel, float* param, float* momentum_buf,
-                                        float lr, float momentum, float weight_decay,
-                                        float* grad_out, uint32_t flags, void* stream) {
+static int allreduce_sgd_impl(const void* const* replicas, int32_t n_replicas, int32_t in_dtype, int64_t numel,
+                              float* param, float* momentum_buf, float lr, float momentum, float weight_decay,
+                              float* grad_out, void* param_bf16, uint32_t flags, void* stream) {
     int st = check_replicas(replicas, n_replicas, in_dtype, numel);
     if (st != DDP_OK) return st;
     if (flags != 0 || (param == nullptr && numel > 0)) return DDP_ERR_INVALID_ARG;
@@ -414,17 +422,19 @@ extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_r
     const bool has_mom = momentum != 0.0f;
     if (has_mom && momentum_buf == nullptr && numel > 0) return DDP_ERR_INVALID_ARG;
     if (!has_mom && momentum_buf != nullptr) return DDP_ERR_INVALID_ARG;
-    if (!aligned16(param) || (momentum_buf && !aligned16(momentum_buf)) || (grad_out && !aligned16(grad_out)))
+    if (!aligned16(param) || (momentum_buf && !aligned16(momentum_buf)) || (grad_out && !aligned16(grad_out)) ||
+        !aligned16(param_bf16))
         return DDP_ERR_ALIGNMENT;
     const size_t esz = in_dtype == DDP_BF16 ? 2 : 4;
     const size_t in_bytes = static_cast<size_t>(numel) * esz, fb = static_cast<size_t>(numel) * 4;
-    const void* outs[3] = {param, momentum_buf, grad_out};
-    for (int i = 0; i < 3; ++i) {
+    const void* outs[4] = {param, momentum_buf, grad_out, param_bf16};
+    const size_t ob[4] = {fb, fb, fb, static_cast<size_t>(numel) * 2};
+    for (int i = 0; i < 4; ++i) {
         if (outs[i] == nullptr) continue;
         for (int j = 0; j < i; ++j)
-            if (outs[j] != nullptr && overlaps(outs[i], fb, outs[j], fb)) return DDP_ERR_INVALID_ARG;
+            if (overlaps(outs[i], ob[i], outs[j], ob[j])) return DDP_ERR_INVALID_ARG;
         for (int r = 0; r < n_replicas; ++r)
-            if (overlaps(outs[i], fb, replicas[r], in_bytes)) return DDP_ERR_INVALID_ARG;
+            if (overlaps(outs[i], ob[i], replicas[r], in_bytes)) return DDP_ERR_INVALID_ARG;
     }
     if (numel == 0) return DDP_OK;
 
@@ -433,6 +443,7 @@ extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_r
     p.param = param;
     p.buf = momentum_buf;
     p.gout = grad_out;
+    p.lowp = static_cast<__nv_bfloat16*>(param_bf16);
     p.numel = numel;
     p.n = n_replicas;
     p.pow2 = is_pow2(n_replicas);
@@ -445,6 +456,23 @@ extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_r
     return in_dtype == DDP_BF16 ? dispatch_sgd<true>(p, nvec, s) : dispatch_sgd<false>(p, nvec, s);
 }
 
+
+extern "C" int ddp_bucket_allreduce_sgd(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                                        int64_t numel, float* param, float* momentum_buf,
+                                        float lr, float momentum, float weight_decay,
+                                        float* grad_out, uint32_t flags, void* stream) {
+    return allreduce_sgd_impl(replicas, n_replicas, in_dtype, numel, param, momentum_buf, lr, momentum, weight_decay,
+                              grad_out, nullptr, flags, stream);
+}
+
+extern "C" int ddp_bucket_allreduce_sgd_cast(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                                             int64_t numel, float* param, float* momentum_buf, float lr,
+                                             float momentum, float weight_decay, float* grad_out, void* param_bf16,
+                                             void* stream) {
+    if (param_bf16 == nullptr && numel > 0) return DDP_ERR_INVALID_ARG;
+    return allreduce_sgd_impl(replicas, n_replicas, in_dtype, numel, param, momentum_buf, lr, momentum, weight_decay,
+                              grad_out, param_bf16, 0u, stream);
+}
 
 // ---------------------------------------------------------------- average with a norm side output
 

@@ -37,6 +37,18 @@ __device__ __forceinline__ void st16(void* p, uint4 v) {
                  : "memory");
 }
 
+// 8-byte streaming store.
+__device__ __forceinline__ void st8(void* p, uint2 v) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// Two fp32 values rounded to bf16 (nearest, ties to even), element 0 in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    return l | (h << 16);
+}
+
 __device__ __forceinline__ uint4 f4_bits(float a, float b, float c, float d) {
     return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
 }

@@ -467,12 +467,6 @@ __device__ __forceinline__ float normalize(float x, float4 k) {
     return fmaf(__fsub_rn(__fsub_rn(x, k.x), k.y), k.z, k.w);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
-}
-
 __device__ __forceinline__ uint32_t channel_of(uint32_t e, const BnParams& a) {
     const uint32_t pl = fdiv(e, a.div_hw);
     return pl - fdiv(pl, a.div_c) * static_cast<uint32_t>(a.C);

@@ -246,9 +246,27 @@ int ddp_grad_norm_finalize(const void* norm_ws, int32_t n_buckets, float max_nor
  *   param, momentum_buf, lr, momentum, weight_decay   as ddp_bucket_allreduce_sgd
  *   grad_scale    device float or NULL, e.g. clip_coef_out of
  *                 ddp_grad_norm_finalize
+ *   param_bf16    device bf16[numel] or NULL: also store the updated θ
+ *                 rounded to bf16 (as ddp_bucket_allreduce_sgd_cast)
  */
 int ddp_bucket_sgd(const float* grad, float* param, float* momentum_buf, int64_t numel, float lr,
-                   float momentum, float weight_decay, const float* grad_scale, void* stream);
+                   float momentum, float weight_decay, const float* grad_scale, void* param_bf16, void* stream);
+
+/*
+ * ddp_bucket_allreduce_sgd_cast — ddp_bucket_allreduce_sgd that also stores
+ * the updated θ rounded to bf16 (nearest, ties to even) into param_bf16.
+ *
+ * [TR16] §六: master weights are FP32, the compute copy half width, and one
+ * whole-region cast refreshes the compute copy after the update.  Writing
+ * the copy from the update kernel costs its 2-byte store per element and
+ * saves the cast pass (a 4-byte read and the same store).
+ *   param_bf16    device bf16[numel], 16-byte aligned, overlapping nothing
+ *                 else of the call
+ * flags are not taken.
+ */
+int ddp_bucket_allreduce_sgd_cast(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
+                                  int64_t numel, float* param, float* momentum_buf, float lr, float momentum,
+                                  float weight_decay, float* grad_out, void* param_bf16, void* stream);
 
 /*
  * syncbn_workspace_bytes — device workspace that syncbn_merge_apply needs

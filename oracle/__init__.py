@@ -18,6 +18,7 @@ from .ddp_oracle import (  # noqa: F401
     bn_running_update,
     clip_coefficient,
     dist_sampler_indices,
+    f32_to_bf16_rne,
     f64_to_bf16_rne,
     feistel_encrypt,
     grad_mean,

@@ -540,3 +540,15 @@ def bn_fold_inference(running_mean, running_var, gamma, beta, eps: float):
     b = np.zeros_like(rm) if beta is None else np.asarray(beta, np.float64)
     scale = g / np.sqrt(rv + eps)
     return scale, b - rm * scale
+
+
+def f32_to_bf16_rne(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bit patterns (uint16), round to nearest, ties to even; a
+    NaN stays a NaN.  The low-precision copy of the updated master weights
+    ([TR16] §六: FP32 master weights and a half-width compute copy, refreshed
+    by one whole-region cast after the update)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = (u & 0x7FFFFFFF) > 0x7F800000
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    r = np.where(nan, (u >> 16) | 0x40, r)
+    return r.astype(np.uint16)

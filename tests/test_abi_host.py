@@ -241,18 +241,21 @@ def test_accum_clip_rejects(g):
     assert f(FAKE, 1, 1.0, FAKE + 16, None, None, None) == g.DDP_ERR_INVALID_ARG          # output inside ws
     s = lib.ddp_bucket_sgd
     G, P, B = FAKE, FAKE + 4096, FAKE + 8192
-    assert s(G, P, None, 8, 0.1, 0.9, 0.0, None, None) == g.DDP_ERR_INVALID_ARG          # needs the buffer
-    assert s(G, P, B, 8, 0.1, 0.0, 0.0, None, None) == g.DDP_ERR_INVALID_ARG             # buffer unused
-    assert s(G, G + 16, B, 8, 0.1, 0.9, 0.0, None, None) == g.DDP_ERR_INVALID_ARG        # θ overlaps grad
-    assert s(G, P + 4, B, 8, 0.1, 0.9, 0.0, None, None) == g.DDP_ERR_ALIGNMENT
-    assert s(G, P, B, 0, 0.1, 0.9, 0.0, None, None) == g.DDP_OK
+    assert s(G, P, None, 8, 0.1, 0.9, 0.0, None, None, None) == g.DDP_ERR_INVALID_ARG    # needs the buffer
+    assert s(G, P, B, 8, 0.1, 0.0, 0.0, None, None, None) == g.DDP_ERR_INVALID_ARG       # buffer unused
+    assert s(G, G + 16, B, 8, 0.1, 0.9, 0.0, None, None, None) == g.DDP_ERR_INVALID_ARG  # θ overlaps grad
+    assert s(G, P + 4, B, 8, 0.1, 0.9, 0.0, None, None, None) == g.DDP_ERR_ALIGNMENT
+    assert s(G, P, B, 8, 0.1, 0.9, 0.0, None, P + 16, None) == g.DDP_ERR_INVALID_ARG     # bf16 copy on θ
+    assert s(G, P, B, 0, 0.1, 0.9, 0.0, None, None, None) == g.DDP_OK
 
 
 def test_absent_buffers_never_overlap(g):
     """NULL optional outputs (no momentum buffer, no scale) are accepted."""
     lib = g.lib_handle()
-    assert lib.ddp_bucket_sgd(FAKE, FAKE + 4096, None, 0, 0.1, 0.0, 0.0, None, None) == g.DDP_OK
     two = _ptrs(FAKE, FAKE + 4096)
+    assert lib.ddp_bucket_sgd(FAKE, FAKE + 4096, None, 0, 0.1, 0.0, 0.0, None, None, None) == g.DDP_OK
+    assert lib.ddp_bucket_allreduce_sgd_cast(two, 2, 0, 8, FAKE + 8192, None, 0.1, 0.0, 0.0, None, None,
+                                             None) == g.DDP_ERR_INVALID_ARG                 # cast needs its output
     assert lib.ddp_bucket_allreduce_sgd(two, 2, 0, 0, FAKE + 8192, None, 0.1, 0.0, 0.0, None, 0, None) == g.DDP_OK
 
 

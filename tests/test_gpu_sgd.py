@@ -100,3 +100,41 @@ def test_gpt2_deep_first_full_size_sampled(g):
         assert_bit_exact(theta[idx_d], th_w, f"theta step {step}")
         assert_bit_exact(buf[idx_d], b_w, f"buf step {step}")
         del reps
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sgd_with_bf16_weight_copy(g, dtype):
+    """ddp_bucket_allreduce_sgd_cast: θ as without the copy, and the copy is
+    θ rounded to bf16 (nearest, ties to even), bit for bit."""
+    for n in (1, 3, 8):
+        for numel in (1, 3, 4, 5, 8, 9, 4099, 250_007):
+            gen = np.random.Generator(np.random.PCG64(n * 13 + numel))
+            theta = (gen.standard_normal(numel) * 0.02).astype(np.float32)
+            buf = np.zeros(numel, np.float32)
+            reps = [(gen.standard_normal(numel) * 0.01).astype(np.float32) for _ in range(n)]
+            if dtype == "bf16":
+                reps = [workloads.f32_to_bf16_bits(r) for r in reps]
+            d = [dev_f32(r) if dtype == "f32" else dev_bf16(r) for r in reps]
+            th_d, b_d = dev_f32(theta), dev_f32(buf)
+            low = torch.empty(numel, dtype=torch.bfloat16, device="cuda")
+            g.ddp_bucket_allreduce_sgd_cast(d, th_d, b_d, 0.1, 0.9, 1e-4, low)
+            sync()
+            th_w, b_w, _ = oracle.sgd_step(reps, theta, buf, 0.1, 0.9, 1e-4, dtype=dtype)
+            assert_bit_exact(th_d, th_w, f"theta {dtype} N={n} numel={numel}")
+            got = low.view(torch.int16).cpu().numpy().view(np.uint16)
+            np.testing.assert_array_equal(got, oracle.f32_to_bf16_rne(th_w))
+
+
+def test_sgd_from_grad_with_bf16_weight_copy(g):
+    gen = np.random.Generator(np.random.PCG64(77))
+    for numel in (1, 6, 4099, 300_001):
+        gr = (gen.standard_normal(numel) * 0.05).astype(np.float32)
+        th = (gen.standard_normal(numel) * 0.02).astype(np.float32)
+        th_d = dev_f32(th)
+        low = torch.empty(numel, dtype=torch.bfloat16, device="cuda")
+        sc = torch.tensor([0.5], device="cuda")
+        g.ddp_bucket_sgd(dev_f32(gr), th_d, None, 0.1, 0.0, 1e-4, grad_scale=sc, param_bf16=low)
+        sync()
+        th_w, _ = oracle.sgd_from_grad(gr, th, None, 0.1, 0.0, 1e-4, scale=np.float32(0.5))
+        assert_bit_exact(th_d, th_w, f"theta numel={numel}")
+        np.testing.assert_array_equal(low.view(torch.int16).cpu().numpy().view(np.uint16), oracle.f32_to_bf16_rne(th_w))

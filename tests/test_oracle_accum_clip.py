@@ -107,3 +107,19 @@ def test_sgd_from_grad_matches_sgd_step():
     th3, b3 = oracle.sgd_from_grad(np.array([2.0], np.float32), np.array([1.0], np.float32), None,
                                    0.5, 0.0, 0.0, scale=0.25)
     assert th3[0] == 0.75 and b3 is None
+
+
+def test_f32_to_bf16_rne_vs_torch():
+    """Every class of value against torch's fp32 -> bf16 conversion: random
+    magnitudes, exact ties (both parities), the largest values that still
+    round to finite, subnormals, signed zeros, infinities; NaN stays NaN."""
+    gen = np.random.Generator(np.random.PCG64(21))
+    x = (gen.standard_normal(100_000) * np.exp(gen.uniform(-80, 80, 100_000))).astype(np.float32)
+    ties = np.array([0x3F808000, 0x3F818000, 0xBF808000, 0x00008000, 0x00018000, 0x7F7F8000, 0x7F7F7FFF],
+                    np.uint32).view(np.float32)
+    special = np.array([0.0, -0.0, np.inf, -np.inf, 1e-45, -1e-45, 3.4e38], np.float32)
+    x = np.concatenate([x, ties, special])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(oracle.f32_to_bf16_rne(x), want)
+    nanbits = oracle.f32_to_bf16_rne(np.array([np.nan], np.float32))
+    assert np.isnan(oracle.bf16_bits_to_f32(nanbits))[0]
