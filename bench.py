@@ -384,33 +384,51 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     per_bucket_us = [ea.elapsed_time(eb) / 20 * 1e3 for ea, eb in per_bucket_us]
 
-    # end to end through the public API: pinned host replicas -> HBM, 5 bucket calls, result -> pinned host
+    # End to end through the public API, host buffers in and out, two ways:
+    #  "copy":      copy-engine copies of the replicas from pinned host memory into HBM, the 5 bucket calls on
+    #               device buffers, the result copied back to pinned host memory;
+    #  "zero-copy": the same 5 bucket calls given the pinned host buffers themselves — the kernels read the
+    #               replicas over NVLink-C2C (coherent host memory) and write the average to host memory.
     host_reps = [torch.empty(total, dtype=torch.float32, pin_memory=True) for _ in range(N_REPLICAS)]
     for h, d in zip(host_reps, reps):
         h.copy_(d)
     host_out = torch.empty(total, dtype=torch.float32, pin_memory=True)
     torch.cuda.synchronize()
 
-    def e2e_step():
+    def launch_host(b):
+        off, n = buckets[b][0], buckets[b][1]
+        g.ddp_bucket_allreduce_mean([x[off:off + n] for x in host_reps], host_out[off:off + n])
+
+    def e2e_copy_step():
         for h, d in zip(host_reps, reps):
             d.copy_(h, non_blocking=True)
         for b in range(nb):
             launch(b)
         host_out.copy_(out, non_blocking=True)
 
-    with torch.cuda.stream(side):
-        e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(side):
-        e0.record()
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record()
-    torch.cuda.synchronize()
-    e2e_value = weak_scaling_rate(world, step_bytes, args.e2e_steps, dist_max(e0.elapsed_time(e1), world, dev))
+    def e2e_zero_copy_step():
+        for b in range(nb):
+            launch_host(b)
+
+    def time_e2e(fn):
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(side):
+            e0.record()
+            for _ in range(args.e2e_steps):
+                fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return weak_scaling_rate(world, step_bytes, args.e2e_steps, dist_max(e0.elapsed_time(e1), world, dev))
+
+    e2e_copy = time_e2e(e2e_copy_step)
+    e2e_zero = time_e2e(e2e_zero_copy_step)
+    host_check = bool(torch.equal(host_out, out.cpu()))      # both modes computed the same average
+    e2e_value, e2e_mode = (e2e_zero, "zero-copy") if e2e_zero >= e2e_copy else (e2e_copy, "copy")
 
     rows = None
     if rank == 0 and world == 1 and not args.no_rows:
@@ -437,7 +455,9 @@ def run_ours(args, world, rank, local):
                          **({"traffic_note": traffic_note} if traffic_note else {})},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": N_REPLICAS * total * 4,
-                    "d2h_bytes_per_step": total * 4, "steps": args.e2e_steps},
+                    "d2h_bytes_per_step": total * 4, "steps": args.e2e_steps, "mode": e2e_mode,
+                    "copy_mode_value": e2e_copy, "zero_copy_mode_value": e2e_zero,
+                    "modes_agree_bitwise": host_check},
             "gpu_launches": K * nb,
             "clocks": clocks,
         }
