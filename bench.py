@@ -612,6 +612,30 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                                 "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
                                 "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
                                 "launches": 1}
+    # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point)
+    sweep = []
+    for size in (4 << 20, 64 << 20, 1 << 30):
+        numel = size // 4
+        for n in (2, 8, 16):
+            reps = [workloads.device_normal((numel,), 0.0, 1.0, workloads.seed_for(5, r), device=dev)
+                    for r in range(n)]
+            outs = torch.empty(numel, device=dev)
+            for cap in (1 << 20, 25 << 20, 100 << 20):
+                ce = cap // 4
+
+                def flat_step(reps=reps, outs=outs, ce=ce, numel=numel):
+                    for s0 in range(0, numel, ce):
+                        e = min(numel, s0 + ce)
+                        g.ddp_bucket_allreduce_mean([x[s0:e] for x in reps], outs[s0:e])
+                iters = 200 if size <= (64 << 20) else 20
+                ms = _time_launches(torch, flat_step, iters, side)
+                nbytes = (n + 1) * size
+                sweep.append({"bytes_per_replica": size, "replicas": n, "cap_mib": cap >> 20,
+                              "launches": -(-numel // ce), "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
+                              "frac": nbytes / ms / 1e6 / peak,
+                              "l2": "working set in L2" if (n + 1) * size < L2_BYTES else "larger than L2"})
+            del reps, outs
+    rows["sweep_flat_fp32"] = sweep
     rows["_peak"] = {"hbm_gbs": peak, "source": peak_kind}
     return rows
 

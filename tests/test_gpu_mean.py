@@ -201,3 +201,30 @@ def test_sweep_chunked_flat_buffers(g):
                     g.ddp_bucket_allreduce_mean([x[s:e] for x in d], out[s:e])
                 sync()
                 assert_bit_exact(out, want, f"sweep {size_bytes}B N={n} cap={cap}")
+
+
+def test_sweep_full_size_sampled(g):
+    """Flat fp32 buffers of 1 GiB (268,435,456 elements), N in {2, 16}, split
+    into cap-sized bucket launches (1, 25, 100 MiB) as the benchmark sweep
+    launches them; inputs drawn on the device from seeded generators, 2^20
+    sampled outputs plus both ends of every bucket recomputed by the oracle."""
+    numel = (1 << 30) // 4
+    gen = np.random.Generator(np.random.PCG64(51))
+    for n in (2, 16):
+        reps = [workloads.device_normal((numel,), 0.0, 1.0, workloads.seed_for(5, r) + 17 * n) for r in range(n)]
+        for cap in (1 * MiB, 25 * MiB, 100 * MiB):
+            ce = cap // 4
+            out = torch.empty(numel, device="cuda")
+            starts = list(range(0, numel, ce))
+            for s in starts:
+                e = min(numel, s + ce)
+                g.ddp_bucket_allreduce_mean([x[s:e] for x in reps], out[s:e])
+            idx = [gen.integers(0, numel, 1 << 20)]
+            for s in starts[:: max(1, len(starts) // 64)]:
+                idx += [np.arange(s, min(numel, s + 8)), np.arange(max(0, s - 8), s)]
+            idx = np.unique(np.concatenate(idx))
+            idx_d = torch.from_numpy(idx).cuda()
+            sync()
+            want = oracle.grad_mean([x[idx_d].cpu().numpy() for x in reps])
+            assert_bit_exact(out[idx_d], want, f"sweep 1 GiB N={n} cap={cap >> 20} MiB")
+        del reps
