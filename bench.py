@@ -634,6 +634,18 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                               "launches": -(-numel // ce), "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
                               "frac": nbytes / ms / 1e6 / peak,
                               "l2": "working set in L2" if (n + 1) * size < L2_BYTES else "larger than L2"})
+                if cap == (1 << 20):
+                    # the same buckets averaged by one grouped launch (up to 1024 buckets per launch)
+                    bl = [(s0, min(ce, numel - s0)) for s0 in range(0, numel, ce)]
+
+                    def grouped(reps=reps, outs=outs, bl=bl):
+                        for i in range(0, len(bl), 1024):
+                            g.ddp_bucket_allreduce_mean_multi(reps, bl[i:i + 1024], outs)
+                    ms = _time_launches(torch, grouped, iters, side)
+                    sweep.append({"bytes_per_replica": size, "replicas": n, "cap_mib": 1,
+                                  "launches": -(-len(bl) // 1024), "grouped": True, "us": ms * 1e3,
+                                  "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+                                  "l2": "working set in L2" if (n + 1) * size < L2_BYTES else "larger than L2"})
             del reps, outs
     rows["sweep_flat_fp32"] = sweep
     rows["_peak"] = {"hbm_gbs": peak, "source": peak_kind}

@@ -371,3 +371,26 @@ def ddp_bucket_allreduce_sgd_cast(replicas, param, momentum_buf, lr: float, mome
 
 
 __all__ += ["ddp_bucket_allreduce_sgd_cast"]
+
+
+MULTI_MAX_BUCKETS = 1024
+_lib.ddp_bucket_allreduce_mean_multi.argtypes = [_P, _c.c_int32, _c.c_int32, _P, _c.c_int32, _P, _P]
+_lib.ddp_bucket_allreduce_mean_multi.restype = _c.c_int
+
+
+def ddp_bucket_allreduce_mean_multi(replica_bases, buckets, out_base, stream=None) -> None:
+    """Average several buckets (list of (offset_elems, numel, ...)) of one
+    flat layout in one launch; same bits as one call per bucket."""
+    if not 1 <= len(replica_bases) <= MAX_REPLICAS:
+        raise ValueError("need 1..16 replicas")
+    nb = len(buckets)
+    arr = (DdpBucket * max(1, nb))()
+    for i, b in enumerate(buckets):
+        arr[i].offset_elems, arr[i].numel = int(b[0]), int(b[1])
+    _check(_lib.ddp_bucket_allreduce_mean_multi(_ptr_array(replica_bases), len(replica_bases),
+                                                _dtype_code(replica_bases[0]), ctypes.addressof(arr), nb,
+                                                _ptr(out_base), _stream_ptr(stream)),
+           "ddp_bucket_allreduce_mean_multi")
+
+
+__all__ += ["ddp_bucket_allreduce_mean_multi", "MULTI_MAX_BUCKETS"]

@@ -529,3 +529,143 @@ extern "C" int ddp_bucket_allreduce_mean_norm(const void* const* replicas, int32
     return in_dtype == DDP_BF16 ? dispatch_mean_norm<true>(p, nvec, s, aliased)
                                 : dispatch_mean_norm<false>(p, nvec, s, aliased);
 }
+
+// ---------------------------------------------------------------- several buckets in one launch
+
+namespace ddp {
+namespace {
+
+constexpr int kMultiMaxBuckets = DDP_MULTI_MAX_BUCKETS;
+constexpr int kChunk = 128;                 // vectors per warp chunk (4 per lane)
+
+struct MultiParams {
+    RepPtrs rep;                            // replica flat-buffer bases
+    float* out;                             // output flat-buffer base
+    int32_t n;
+    int32_t pow2;
+    float inv_n;
+    int32_t n_buckets;
+    int64_t off[kMultiMaxBuckets];          // bucket offsets (elements)
+    int64_t numel[kMultiMaxBuckets];
+    int32_t chunk_start[kMultiMaxBuckets + 1];   // prefix sums of chunks per bucket
+};
+
+template <int NMAX, bool BF16>
+__global__ void __launch_bounds__(kThreads) mean_multi_kernel(const __grid_constant__ MultiParams a) {
+    constexpr int VEC = BF16 ? 8 : 4;
+    constexpr int ESZ = BF16 ? 2 : 4;
+    const int n = a.n;
+    const int lane = threadIdx.x % 32;
+    const int warps = gridDim.x * (kThreads / 32);
+    const int total = a.chunk_start[a.n_buckets];
+    pdl_enter();
+    for (int c = blockIdx.x * (kThreads / 32) + threadIdx.x / 32; c < total; c += warps) {
+        int lo = 0, hi = a.n_buckets - 1;    // bucket b with chunk_start[b] <= c < chunk_start[b+1] (warp-uniform)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) / 2;
+            if (a.chunk_start[mid] <= c) lo = mid;
+            else hi = mid - 1;
+        }
+        const int b = lo;
+        const int64_t off = a.off[b], numel = a.numel[b];
+        const int64_t nvec = numel / VEC;
+        const int64_t v0 = static_cast<int64_t>(c - a.chunk_start[b]) * kChunk;
+#pragma unroll 1
+        for (int j = 0; j < kChunk / 32; ++j) {
+            const int64_t v = v0 + j * 32 + lane;
+            if (v >= nvec) break;
+            const int64_t e0 = off + v * VEC;
+            uint4 raw[NMAX];
+#pragma unroll
+            for (int r = 0; r < NMAX; ++r)
+                if (r < n) raw[r] = ld16<true>(static_cast<const char*>(a.rep.p[r]) + e0 * ESZ);
+            float res[VEC];
+#pragma unroll
+            for (int k = 0; k < VEC; ++k) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int r = 0; r < NMAX; ++r)
+                    if (r < n) acc = __fadd_rn(acc, vec_elem<BF16>(raw[r], k));
+                res[k] = scale_by_n(acc, a.pow2, a.inv_n, n);
+            }
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q)
+                st16(a.out + e0 + 4 * q, f4_bits(res[4 * q], res[4 * q + 1], res[4 * q + 2], res[4 * q + 3]));
+        }
+        // the bucket's last chunk also averages its ragged tail
+        if (c == a.chunk_start[b + 1] - 1 && lane < numel - nvec * VEC) {
+            const int64_t e = off + nvec * VEC + lane;
+            float acc = 0.0f;
+            for (int r = 0; r < n; ++r) acc = __fadd_rn(acc, load_elem<BF16>(a.rep.p[r], e));
+            a.out[e] = scale_by_n(acc, a.pow2, a.inv_n, n);
+        }
+    }
+}
+
+template <bool BF16>
+int dispatch_multi(const MultiParams& p, int64_t total_chunks, cudaStream_t s) {
+    void (*kernel)(MultiParams) = p.n <= 4 ? mean_multi_kernel<4, BF16>
+                                : p.n <= 8 ? mean_multi_kernel<8, BF16> : mean_multi_kernel<16, BF16>;
+    int grid = 0;
+    const int64_t need = (total_chunks + kThreads / 32 - 1) / (kThreads / 32);
+    const int st = one_wave_grid(reinterpret_cast<const void*>(kernel), kThreads, need, &grid);
+    if (st != DDP_OK) return st;
+    return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), kThreads, s, p);
+}
+
+}  // namespace
+}  // namespace ddp
+
+extern "C" int ddp_bucket_allreduce_mean_multi(const void* const* replica_bases, int32_t n_replicas,
+                                               int32_t in_dtype, const ddp_bucket* buckets, int32_t n_buckets,
+                                               float* out_base, void* stream) {
+    if (n_buckets < 0 || n_buckets > DDP_MULTI_MAX_BUCKETS || (n_buckets > 0 && buckets == nullptr))
+        return DDP_ERR_INVALID_ARG;
+    int64_t span = 0;               // elements from the base to the end of the last bucket
+    int64_t prev_end = 0;
+    for (int b = 0; b < n_buckets; ++b) {
+        const int64_t o = buckets[b].offset_elems, m = buckets[b].numel;
+        if (o < 0 || m < 0 || o < prev_end || m > INT64_MAX / 16 - o) return DDP_ERR_INVALID_ARG;
+        prev_end = o + m;
+        span = prev_end;
+    }
+    int st = check_replicas(replica_bases, n_replicas, in_dtype, span);
+    if (st != DDP_OK) return st;
+    if (out_base == nullptr && span > 0) return DDP_ERR_INVALID_ARG;
+    if (!aligned16(out_base)) return DDP_ERR_ALIGNMENT;
+    const int64_t esz = in_dtype == DDP_BF16 ? 2 : 4;
+    for (int b = 0; b < n_buckets; ++b)
+        if ((buckets[b].offset_elems * esz) % 16 != 0 || (buckets[b].offset_elems * 4) % 16 != 0)
+            return DDP_ERR_ALIGNMENT;
+    for (int b = 0; b < n_buckets; ++b) {
+        const int64_t o = buckets[b].offset_elems, m = buckets[b].numel;
+        for (int r = 0; r < n_replicas; ++r)
+            if (overlaps(out_base + o, static_cast<size_t>(m) * 4, replica_bases[r],
+                         static_cast<size_t>(span) * esz))
+                return DDP_ERR_INVALID_ARG;
+    }
+    if (span == 0) return DDP_OK;
+    static thread_local MultiParams p;      // ~20 KB: kept off the stack
+    p = MultiParams{};
+    for (int r = 0; r < n_replicas; ++r) p.rep.p[r] = replica_bases[r];
+    p.out = out_base;
+    p.n = n_replicas;
+    p.pow2 = is_pow2(n_replicas);
+    p.inv_n = 1.0f / static_cast<float>(n_replicas);
+    p.n_buckets = n_buckets;
+    const int64_t vec = in_dtype == DDP_BF16 ? 8 : 4;
+    int64_t chunks = 0;
+    for (int b = 0; b < n_buckets; ++b) {
+        p.off[b] = buckets[b].offset_elems;
+        p.numel[b] = buckets[b].numel;
+        p.chunk_start[b] = static_cast<int32_t>(chunks);
+        const int64_t nv = buckets[b].numel / vec;
+        chunks += buckets[b].numel == 0 ? 0 : (nv == 0 ? 1 : (nv + kChunk - 1) / kChunk +
+                                                            ((buckets[b].numel % vec) != 0 && nv % kChunk == 0 ? 1 : 0));
+        if (chunks > INT32_MAX / 2) return DDP_ERR_UNSUPPORTED;
+    }
+    p.chunk_start[n_buckets] = static_cast<int32_t>(chunks);
+    if (chunks == 0) return DDP_OK;        // only empty buckets
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return in_dtype == DDP_BF16 ? dispatch_multi<true>(p, chunks, s) : dispatch_multi<false>(p, chunks, s);
+}

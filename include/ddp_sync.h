@@ -150,6 +150,31 @@ int ddp_plan_buckets(int32_t n_tensors, const int64_t* numels, int32_t elem_byte
 int ddp_bucket_allreduce_mean(const void* const* replicas, int32_t n_replicas, int32_t in_dtype,
                               int64_t numel, float* out, uint32_t flags, void* stream);
 
+#define DDP_MULTI_MAX_BUCKETS 1024
+
+/*
+ * ddp_bucket_allreduce_mean_multi — ddp_bucket_allreduce_mean (rank order)
+ * for several buckets of one flat layout in a single launch.
+ *
+ * [DDP] §3.2 and [TR24] §三: small buckets mean many launches; when several
+ * buckets are ready at the same time (the end of backward, the FIRST bucket
+ * of [TR24] §八 together with late DEEP tensors, a sweep of small caps) one
+ * launch serves them all and pays the launch latency once.  The result is
+ * bit for bit that of one ddp_bucket_allreduce_mean call per bucket.
+ *   replica_bases  host array of n_replicas device pointers: each replica's
+ *                  flat gradient buffer (16-byte aligned)
+ *   buckets        host ddp_bucket[n_buckets] in increasing, non-overlapping
+ *                  offset order (e.g. a plan's buckets; first/count unused);
+ *                  offset_elems·4 and offset_elems·elem_bytes must be
+ *                  multiples of 16 (planned 256-byte offsets are)
+ *   n_buckets      0 .. DDP_MULTI_MAX_BUCKETS
+ *   out_base       device float*: the flat output buffer; bucket b's average
+ *                  goes to out_base + offset_elems; must not overlap the
+ *                  replicas (no in-place form)
+ */
+int ddp_bucket_allreduce_mean_multi(const void* const* replica_bases, int32_t n_replicas, int32_t in_dtype,
+                                    const ddp_bucket* buckets, int32_t n_buckets, float* out_base, void* stream);
+
 /*
  * ddp_bucket_allreduce_sgd — average one bucket and apply the SGD step.
  *

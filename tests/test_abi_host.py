@@ -272,3 +272,31 @@ def test_bn_stats_rejects(g):
     assert f(A, B, None, None, -1.0, 8, C, D, None) == g.DDP_ERR_INVALID_ARG
     assert f(A, B, None, None, 1e-5, 8, A, D, None) == g.DDP_ERR_INVALID_ARG   # output on an input
     assert f(A, B, None, None, 1e-5, 0, C, D, None) == g.DDP_OK
+
+
+def test_mean_multi_rejects(g):
+    lib = g.lib_handle()
+    two = _ptrs(FAKE, FAKE + (1 << 20))
+    f = lib.ddp_bucket_allreduce_mean_multi
+    Bk = g.DdpBucket
+
+    def bk(*pairs):
+        arr = (Bk * max(1, len(pairs)))()
+        for i, (o, n) in enumerate(pairs):
+            arr[i].offset_elems, arr[i].numel = o, n
+        return ctypes.addressof(arr), arr
+
+    a, keep = bk((0, 10), (64, 5))
+    out = FAKE + (4 << 20)
+    assert f(two, 2, 0, a, -1, out, None) == g.DDP_ERR_INVALID_ARG
+    assert f(two, 2, 0, a, 1025, out, None) == g.DDP_ERR_INVALID_ARG
+    a2, keep2 = bk((64, 5), (0, 10))                                   # not increasing
+    assert f(two, 2, 0, a2, 2, out, None) == g.DDP_ERR_INVALID_ARG
+    a3, keep3 = bk((0, 10), (6, 5))                                    # overlapping
+    assert f(two, 2, 0, a3, 2, out, None) == g.DDP_ERR_INVALID_ARG
+    a4, keep4 = bk((0, 10), (66, 5))                                   # 66*4 bytes: not 16-aligned
+    assert f(two, 2, 0, a4, 2, out, None) == g.DDP_ERR_ALIGNMENT
+    assert f(two, 2, 0, a, 2, FAKE, None) == g.DDP_ERR_INVALID_ARG     # output on replica 0
+    assert f(two, 2, 0, a, 0, out, None) == g.DDP_OK
+    a5, keep5 = bk((0, 0), (64, 0))
+    assert f(two, 2, 0, a5, 2, out, None) == g.DDP_OK                  # empty buckets only

@@ -228,3 +228,48 @@ def test_sweep_full_size_sampled(g):
             want = oracle.grad_mean([x[idx_d].cpu().numpy() for x in reps])
             assert_bit_exact(out[idx_d], want, f"sweep 1 GiB N={n} cap={cap >> 20} MiB")
         del reps
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_multi_bucket_launch_matches_per_bucket(g, dtype):
+    """ddp_bucket_allreduce_mean_multi gives, in one launch, the bits of one
+    call per bucket: ResNet-50 planned at a 1 MiB cap (66 buckets), ragged and
+    tiny buckets, empty buckets, and replica counts of every class."""
+    num = workloads.numels(workloads.resnet50_layout())
+    elem = 4 if dtype == "f32" else 2
+    layouts = [g.ddp_plan_buckets(num, elem, 1 * MiB)]
+    custom = [(0, 5), (64, 0), (64, 1), (128, 4093), (4224, 3), (4352, 130_000)]
+    layouts.append({"buckets": [(o, m, 0, 0) for o, m in custom], "total_elems": 4352 + 130_000})
+    for li, plan in enumerate(layouts):
+        total = plan["total_elems"]
+        for n in (1, 3, 8, 16):
+            reps = _replicas(n, total, dtype, 900 + 10 * n + li)
+            d = _dev(reps, dtype)
+            out = torch.full((total,), float("nan"), device="cuda")
+            g.ddp_bucket_allreduce_mean_multi(d, plan["buckets"], out)
+            sync()
+            got = out.cpu()
+            for off, m, _, _ in plan["buckets"]:
+                if m:
+                    assert_bit_exact(got[off:off + m], oracle.grad_mean([r[off:off + m] for r in reps], dtype),
+                                     f"layout {li} N={n} bucket@{off}")
+            covered = np.zeros(total, bool)
+            for off, m, _, _ in plan["buckets"]:
+                covered[off:off + m] = True
+            assert np.isnan(got.numpy()[~covered]).all()
+
+
+def test_multi_bucket_sweep_full_size_sampled(g):
+    """1 GiB flat buffer at a 1 MiB cap: 1024 buckets in one launch, N = 8."""
+    numel = (1 << 30) // 4
+    ce = MiB // 4
+    buckets = [(s, min(ce, numel - s), 0, 0) for s in range(0, numel, ce)]
+    assert len(buckets) == 1024
+    reps = [workloads.device_normal((numel,), 0.0, 1.0, workloads.seed_for(5, r) + 3) for r in range(8)]
+    out = torch.empty(numel, device="cuda")
+    g.ddp_bucket_allreduce_mean_multi(reps, buckets, out)
+    gen = np.random.Generator(np.random.PCG64(52))
+    idx = np.unique(np.concatenate([gen.integers(0, numel, 1 << 20), np.arange(0, numel, ce), np.arange(ce - 1, numel, ce)]))
+    idx_d = torch.from_numpy(idx).cuda()
+    sync()
+    assert_bit_exact(out[idx_d], oracle.grad_mean([x[idx_d].cpu().numpy() for x in reps]), "multi 1 GiB")
