@@ -44,7 +44,7 @@ CAP_BYTES = 25 * MiB
 METRIC = "bucket allreduce-mean GB/s (HBM bytes moved) & % of HBM roofline, 1×GB300"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 10 ** 6
-SAMPLER_LANE_INSTR_PER_INDEX = 423.0   # ncu, 1,281,167 items over 8 ranks (profiles/sampler_imagenet.md)
+SAMPLER_LANE_INSTR_PER_INDEX = 241.6   # ncu, 1,281,167 items over 8 ranks (profiles/sampler_imagenet.md)
 
 
 def parse_args():

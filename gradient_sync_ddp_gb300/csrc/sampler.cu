@@ -7,14 +7,15 @@
 // to total), and rank r takes positions r, r+N, r+2N, ...
 //
 // The shuffle is a keyed permutation that any thread evaluates for any
-// position on its own: a 4-round balanced Feistel network on 2h bits
-// (h = ceil(ceil(log2 n)/2)), round keys = the first four SplitMix64 outputs
-// from state seed+epoch, round function = the SplitMix64 output mix (Steele,
-// Lea & Flood, OOPSLA 2014) truncated to h bits, and cycle walking (encrypt
-// again while the value is >= n).  Each walk is bounded: after 4096
+// position on its own: a 4-round Feistel network on bits = ceil(log2 n) bits
+// (halves of ceil(bits/2) and floor(bits/2) bits, so the domain is below
+// 2n), round keys = the first four SplitMix64 outputs from state seed+epoch,
+// round function = the SplitMix64 output mix (Steele, Lea & Flood, OOPSLA
+// 2014) truncated to the half's width, and cycle walking (encrypt again
+// while the value is >= n; under two encryptions per index on average).  Each walk is bounded: after 4096
 // encryptions the thread writes -1 and counts the index in a status word
 // instead of looping on.  The kernel is integer-ALU bound (~4 rounds x
-// ~3.3 walks x 2 64-bit multiplies per index); the 8-byte output per index
+// ~1.6 walks x 2 64-bit multiplies per index); the 8-byte output per index
 // is its only memory traffic.  Threads stream through several output slots
 // so that lanes of a warp stay busy although walk lengths differ.
 #include <cstdint>
@@ -34,12 +35,13 @@ struct SamplerParams {
     int32_t* status;
     uint64_t rk[kRounds];
     uint64_t n;          // items
-    uint64_t mask;       // 2^h - 1
+    uint64_t mask_hi;    // 2^h_hi - 1
+    uint64_t mask_lo;    // 2^h_lo - 1
     int64_t ns;          // num_samples
     int64_t count;       // outputs to write
     int32_t N;           // replicas
     int32_t rank;        // -1: all ranks, rank-major
-    int32_t h;
+    int32_t h_lo;        // width of the low half
     int32_t shuffle;
 };
 
@@ -51,16 +53,17 @@ __host__ __device__ __forceinline__ uint64_t mix64(uint64_t z) {
     return z ^ (z >> 31);
 }
 
+// x = (H, L) with H the high ceil(bits/2) bits and L the low floor(bits/2)
+// bits; even rounds H ^= mix64(L ^ k_i) mod 2^|H|, odd rounds L ^= mix64(H ^
+// k_i) mod 2^|L|.  Every round undoes itself, so the pass is a bijection.
 __device__ __forceinline__ uint64_t encrypt(uint64_t x, const SamplerParams& a) {
-    uint64_t L = x >> a.h, R = x & a.mask;
+    uint64_t H = x >> a.h_lo, L = x & a.mask_lo;
 #pragma unroll
     for (int i = 0; i < kRounds; ++i) {
-        const uint64_t F = mix64(R ^ a.rk[i]) & a.mask;
-        const uint64_t t = L ^ F;
-        L = R;
-        R = t;
+        if (i % 2 == 0) H ^= mix64(L ^ a.rk[i]) & a.mask_hi;
+        else L ^= mix64(H ^ a.rk[i]) & a.mask_lo;
     }
-    return (L << a.h) | R;
+    return (H << a.h_lo) | L;
 }
 
 // Position -> unshuffled index for output slot i.
@@ -157,8 +160,9 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     const uint64_t n = static_cast<uint64_t>(n_items);
     int bits = 1;
     while (bits < 63 && (uint64_t(1) << bits) < n) ++bits;   // smallest bits >= 1 with 2^bits >= n
-    p.h = (bits + 1) / 2;
-    p.mask = (uint64_t(1) << p.h) - 1;
+    p.h_lo = bits / 2;
+    p.mask_lo = (uint64_t(1) << p.h_lo) - 1;
+    p.mask_hi = (uint64_t(1) << (bits - p.h_lo)) - 1;
     p.n = n;
     p.ns = ns;
     p.count = count;
@@ -167,7 +171,7 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     p.shuffle = shuffle;
 
     int grid = 0;
-    constexpr int64_t kSlotsPerThread = 8;
+    constexpr int64_t kSlotsPerThread = 4;
     const int st = one_wave_grid(reinterpret_cast<const void*>(sampler_kernel), kThreads,
                                  (count + kSlotsPerThread * kThreads - 1) / (kSlotsPerThread * kThreads), &grid);
     if (st != DDP_OK) return st;

@@ -57,7 +57,7 @@ namespace {
 constexpr int kTargetCtas = 2048;        // stats CTAs aimed for (about two waves on 152 SMs)
 constexpr int64_t kMaxPartials = 65536;  // C*S bound: fp32 partials stay <= 512 KiB
 constexpr int kRunElems = 2048;          // channels per group: G*H*W <= this (G >= 1)
-constexpr int kStageBytes = 24576;       // shared staging per group-kernel CTA
+constexpr int kStageBytes = 32768;       // shared staging / segment buffer per CTA
 
 struct BnParams {
     const void* x[DDP_MAX_REPLICAS];
@@ -219,55 +219,77 @@ __global__ void __launch_bounds__(kThreads) bn_stats_segment_kernel(const __grid
             rpre[threadIdx.x] = static_cast<int32_t>(pre);
         }
         __syncthreads();
-        // phase A
+        // phase A: four vectors per thread per iteration, all loads issued before the arithmetic
         const uint32_t total = static_cast<uint32_t>(nr) * vslot;
-        for (uint32_t t = threadIdx.x; t < total; t += kThreads) {
-            const uint32_t j = fdiv(t, a.div_unit);
-            const uint32_t v = t - j * vslot;
-            const int32_t e_start = static_cast<int32_t>(v * W) - rpre[j];
-            if (e_start >= run_elems) continue;
-            const char* ptr = rbase[j] + 16ull * v;
-            const uint32_t e_first = e_start > 0 ? static_cast<uint32_t>(e_start) : 0u;
-            const uint32_t ca = fdiv(e_first, a.div_hw);                  // channel (in group) of the first element
-            const int32_t kb = static_cast<int32_t>((ca + 1) * HW) - e_start;   // elements before the next channel
-            const float Ka = Ks[ca], Kb = Ks[ca + 1];
-            float s_all = 0.0f, q_all = 0.0f, s_hi = 0.0f, q_hi = 0.0f;
-            if (e_start >= 0 && e_start + W <= run_elems) {              // interior vector: no masks
-                const uint4 raw = ld16<true>(ptr);
+        for (uint32_t t0 = threadIdx.x; t0 < total; t0 += 4 * kThreads) {
+            uint4 raw[4];
+            int32_t es[4];
+            uint32_t slot[4];
+            bool interior[4];
 #pragma unroll
-                for (int q = 0; q < W; ++q) {
-                    const bool hi = q >= kb;
-                    const float d = __fsub_rn(vec_elem<BF16>(raw, q), hi ? Kb : Ka);
-                    const float dh = hi ? d : 0.0f;
-                    s_all += d;
-                    q_all = fmaf(d, d, q_all);
-                    s_hi += dh;
-                    q_hi = fmaf(dh, dh, q_hi);
-                }
-            } else {                                                      // first or last vector of the run
-                float xe[W];
-                if (e_start + W <= run_elems) {
-                    const uint4 raw = ld16<true>(ptr);
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t t = t0 + u * kThreads;
+                es[u] = INT32_MAX;
+                interior[u] = false;
+                if (t < total) {
+                    const uint32_t j = fdiv(t, a.div_unit);
+                    const uint32_t v = t - j * vslot;
+                    slot[u] = j * vslot + v;
+                    es[u] = static_cast<int32_t>(v * W) - rpre[j];
+                    const char* ptr = rbase[j] + 16ull * v;
+                    interior[u] = es[u] >= 0 && es[u] + W <= run_elems;
+                    if (interior[u]) raw[u] = ld16<true>(ptr);
+                    else if (es[u] < run_elems) {                         // first or last vector of the run
+                        float xe[W];
+                        if (es[u] + W <= run_elems) {
+                            const uint4 r4 = ld16<true>(ptr);
 #pragma unroll
-                    for (int q = 0; q < W; ++q) xe[q] = vec_elem<BF16>(raw, q);
-                } else {
+                            for (int q = 0; q < W; ++q) xe[q] = vec_elem<BF16>(r4, q);
+                        } else {
 #pragma unroll
-                    for (int q = 0; q < W; ++q) xe[q] = (e_start + q < run_elems) ? load_elem<BF16>(ptr, q) : 0.0f;
-                }
+                            for (int q = 0; q < W; ++q)
+                                xe[q] = (es[u] + q < run_elems) ? load_elem<BF16>(ptr, q) : 0.0f;
+                        }
+                        const uint32_t e_first = es[u] > 0 ? static_cast<uint32_t>(es[u]) : 0u;
+                        const uint32_t ca = fdiv(e_first, a.div_hw);
+                        const int32_t kb = static_cast<int32_t>((ca + 1) * HW) - es[u];
+                        const float Ka = Ks[ca], Kb = Ks[ca + 1];
+                        float s_all = 0.0f, q_all = 0.0f, s_hi = 0.0f, q_hi = 0.0f;
 #pragma unroll
-                for (int q = 0; q < W; ++q) {
-                    const int32_t e = e_start + q;
-                    const bool valid = e >= 0 && e < run_elems;
-                    const bool hi = q >= kb;
-                    const float d = valid ? __fsub_rn(xe[q], hi ? Kb : Ka) : 0.0f;
-                    const float dh = hi ? d : 0.0f;
-                    s_all += d;
-                    q_all = fmaf(d, d, q_all);
-                    s_hi += dh;
-                    q_hi = fmaf(dh, dh, q_hi);
+                        for (int q = 0; q < W; ++q) {
+                            const int32_t e = es[u] + q;
+                            const bool valid = e >= 0 && e < run_elems;
+                            const bool hi = q >= kb;
+                            const float d = valid ? __fsub_rn(xe[q], hi ? Kb : Ka) : 0.0f;
+                            const float dh = hi ? d : 0.0f;
+                            s_all += d;
+                            q_all = fmaf(d, d, q_all);
+                            s_hi += dh;
+                            q_hi = fmaf(dh, dh, q_hi);
+                        }
+                        seg[slot[u]] = make_float4(__fsub_rn(s_all, s_hi), __fsub_rn(q_all, q_hi), s_hi, q_hi);
+                    }
                 }
             }
-            seg[j * vslot + v] = make_float4(__fsub_rn(s_all, s_hi), __fsub_rn(q_all, q_hi), s_hi, q_hi);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (!interior[u]) continue;                               // interior vector: no masks
+                const uint32_t ca = fdiv(static_cast<uint32_t>(es[u]), a.div_hw);
+                const int32_t kb = static_cast<int32_t>((ca + 1) * HW) - es[u];
+                const float Ka = Ks[ca], Kb = Ks[ca + 1];
+                float s_all = 0.0f, q_all = 0.0f, s_hi = 0.0f, q_hi = 0.0f;
+#pragma unroll
+                for (int q = 0; q < W; ++q) {
+                    const bool hi = q >= kb;
+                    const float d = __fsub_rn(vec_elem<BF16>(raw[u], q), hi ? Kb : Ka);
+                    const float dh = hi ? d : 0.0f;
+                    s_all += d;
+                    q_all = fmaf(d, d, q_all);
+                    s_hi += dh;
+                    q_hi = fmaf(dh, dh, q_hi);
+                }
+                seg[slot[u]] = make_float4(__fsub_rn(s_all, s_hi), __fsub_rn(q_all, q_hi), s_hi, q_hi);
+            }
         }
         __syncthreads();
         // phase B

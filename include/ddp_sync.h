@@ -414,10 +414,11 @@ int64_t dist_sampler_num_samples(int64_t n_items, int32_t n_replicas, int32_t dr
  * num_samples·N; the (shuffled) list 0..n-1 is padded by repeating its head
  * up to total (or cut to total with drop_last); rank r takes positions
  * r, r+N, r+2N, ...  The shuffle is a permutation keyed by seed+epoch so
- * every rank agrees without communication: a 4-round balanced Feistel
- * network on 2·ceil(ceil(log2 n)/2) bits whose round keys are the first four
- * SplitMix64 outputs from state seed+epoch and whose round function is the
- * SplitMix64 output mix, with cycle walking into [0, n).
+ * every rank agrees without communication: a 4-round Feistel network on
+ * ceil(log2 n) bits (a high half of ceil(bits/2) bits and a low half of
+ * floor(bits/2) bits, updated alternately) whose round keys are the first
+ * four SplitMix64 outputs from state seed+epoch and whose round function is
+ * the SplitMix64 output mix, with cycle walking into [0, n).
  *
  *   n_items        n >= 0 (< 2^62)
  *   n_replicas     N >= 1

@@ -339,22 +339,31 @@ def splitmix64_stream(state: int, count: int):
 
 
 def _feistel_params(n: int):
+    """Half widths of the network for a domain of n values: bits =
+    ceil(log2 n) (at least 1) split into a high half of ceil(bits/2) bits and
+    a low half of floor(bits/2) bits, so the domain 2^bits is below 2n."""
     bits = max(1, (n - 1).bit_length())      # smallest bits with 2^bits >= n
-    h = (bits + 1) // 2
-    return h, (1 << h) - 1
+    h_lo = bits // 2
+    h_hi = bits - h_lo
+    return h_hi, h_lo, (1 << h_hi) - 1, (1 << h_lo) - 1
 
 
 def feistel_encrypt(x: int, key: int, n: int) -> int:
-    """One pass of the keyed balanced Feistel network on 2h bits, where h is
-    half of ceil(log2 n) rounded up.  Round keys are the first four SplitMix64
-    outputs from state ``key``; round i maps (L, R) -> (R, L xor
-    (mix64(R xor k_i) mod 2^h)).  Any round function gives a bijection."""
-    h, mask = _feistel_params(n)
+    """One pass of the keyed Feistel network on bits = ceil(log2 n) bits.
+    x is split into a high half H (ceil(bits/2) bits) and a low half L
+    (floor(bits/2) bits); round keys k_0..k_3 are the first four SplitMix64
+    outputs from state ``key``; even rounds set H ^= mix64(L ^ k_i) mod 2^|H|,
+    odd rounds L ^= mix64(H ^ k_i) mod 2^|L|.  Each round undoes itself, so
+    the pass is a bijection of [0, 2^bits) whatever the round function."""
+    h_hi, h_lo, m_hi, m_lo = _feistel_params(n)
     rk = splitmix64_stream(key, FEISTEL_ROUNDS)
-    L, R = x >> h, x & mask
+    H, L = x >> h_lo, x & m_lo
     for i in range(FEISTEL_ROUNDS):
-        L, R = R, L ^ (splitmix64_mix(R ^ rk[i]) & mask)
-    return (L << h) | R
+        if i % 2 == 0:
+            H ^= splitmix64_mix(L ^ rk[i]) & m_hi
+        else:
+            L ^= splitmix64_mix(H ^ rk[i]) & m_lo
+    return (H << h_lo) | L
 
 
 def keyed_perm(j: int, key: int, n: int) -> int:
@@ -383,10 +392,9 @@ def keyed_perm_all(key: int, n: int) -> np.ndarray:
     (same arithmetic on uint64 lanes; wrapping multiplication mod 2^64)."""
     if n <= 1:
         return np.arange(n, dtype=np.int64)
-    h, mask = _feistel_params(n)
+    h_hi, h_lo, m_hi, m_lo = _feistel_params(n)
     rk = [np.uint64(k) for k in splitmix64_stream(key, FEISTEL_ROUNDS)]
-    m = np.uint64(mask)
-    hh = np.uint64(h)
+    mh, ml, hl = np.uint64(m_hi), np.uint64(m_lo), np.uint64(h_lo)
 
     def mix(z):
         z = z ^ (z >> np.uint64(30))
@@ -396,10 +404,13 @@ def keyed_perm_all(key: int, n: int) -> np.ndarray:
         return z ^ (z >> np.uint64(31))
 
     def enc(x):
-        L, R = x >> hh, x & m
+        H, L = x >> hl, x & ml
         for i in range(FEISTEL_ROUNDS):
-            L, R = R, L ^ (mix(R ^ rk[i]) & m)
-        return (L << hh) | R
+            if i % 2 == 0:
+                H = H ^ (mix(L ^ rk[i]) & mh)
+            else:
+                L = L ^ (mix(H ^ rk[i]) & ml)
+        return (H << hl) | L
 
     with np.errstate(over="ignore"):
         y = enc(np.arange(n, dtype=np.uint64))

@@ -15,14 +15,15 @@ def test_splitmix64_known_answers():
 
 
 def test_feistel_is_a_bijection_on_its_domain():
-    """Every encryption pass permutes [0, 2^(2h)), for every half width up to
-    6 bits and several keys (brute force)."""
+    """Every encryption pass permutes [0, 2^bits), bits = ceil(log2 n), for
+    odd and even widths up to 12 bits and several keys (brute force), and the
+    domain is below 2n."""
     for n in (2, 3, 5, 9, 17, 33, 100, 1000, 3000):
         bits = max(1, (n - 1).bit_length())
-        h = (bits + 1) // 2
+        assert (1 << bits) < 2 * n
         for key in (0, 1, 12345, 2 ** 63 + 7):
-            img = sorted(oracle.feistel_encrypt(x, key, n) for x in range(1 << (2 * h)))
-            assert img == list(range(1 << (2 * h)))
+            img = sorted(oracle.feistel_encrypt(x, key, n) for x in range(1 << bits))
+            assert img == list(range(1 << bits))
 
 
 def check_perm_is_permutation(perm_all, perm_one):
