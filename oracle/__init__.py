@@ -21,11 +21,13 @@ from .ddp_oracle import (  # noqa: F401
     f32_to_bf16_rne,
     f64_to_bf16_rne,
     feistel_encrypt,
+    feistel_round_keys,
     grad_mean,
     grad_global_norm,
     grad_mean_tree,
     keyed_perm,
     keyed_perm_all,
+    murmur3_fmix32,
     plan_buckets,
     ring_allreduce_mean,
     sampler_num_samples,

@@ -312,6 +312,7 @@ def syncbn_stats_at(xs, c: int, eps: float = 1e-5, dtype: str = "bf16"):
 # ---------------------------------------------------------------------------
 
 _M64 = (1 << 64) - 1
+_M32 = (1 << 32) - 1
 SPLITMIX_GAMMA = 0x9E3779B97F4A7C15
 FEISTEL_ROUNDS = 4
 WALK_CAP = 4096
@@ -338,10 +339,28 @@ def splitmix64_stream(state: int, count: int):
     return out
 
 
+def murmur3_fmix32(h: int) -> int:
+    """The 32-bit finalizer of MurmurHash3 (A. Appleby, public domain): two
+    xor-shift / multiply steps and a last xor-shift, on Python ints mod 2^32."""
+    h &= _M32
+    h ^= h >> 16
+    h = (h * 0x85EBCA6B) & _M32
+    h ^= h >> 13
+    h = (h * 0xC2B2AE35) & _M32
+    return h ^ (h >> 16)
+
+
+def feistel_round_keys(key: int):
+    """k_0..k_3: the high 32 bits of the first four SplitMix64 outputs from
+    state ``key``."""
+    return [z >> 32 for z in splitmix64_stream(key, FEISTEL_ROUNDS)]
+
+
 def _feistel_params(n: int):
     """Half widths of the network for a domain of n values: bits =
     ceil(log2 n) (at least 1) split into a high half of ceil(bits/2) bits and
-    a low half of floor(bits/2) bits, so the domain 2^bits is below 2n."""
+    a low half of floor(bits/2) bits, so the domain 2^bits is below 2n.  For
+    n < 2^62 both halves fit in 31 bits."""
     bits = max(1, (n - 1).bit_length())      # smallest bits with 2^bits >= n
     h_lo = bits // 2
     h_hi = bits - h_lo
@@ -351,18 +370,18 @@ def _feistel_params(n: int):
 def feistel_encrypt(x: int, key: int, n: int) -> int:
     """One pass of the keyed Feistel network on bits = ceil(log2 n) bits.
     x is split into a high half H (ceil(bits/2) bits) and a low half L
-    (floor(bits/2) bits); round keys k_0..k_3 are the first four SplitMix64
-    outputs from state ``key``; even rounds set H ^= mix64(L ^ k_i) mod 2^|H|,
-    odd rounds L ^= mix64(H ^ k_i) mod 2^|L|.  Each round undoes itself, so
-    the pass is a bijection of [0, 2^bits) whatever the round function."""
+    (floor(bits/2) bits); with the round keys k_i of feistel_round_keys, even
+    rounds set H ^= fmix32(L ^ k_i) mod 2^|H|, odd rounds L ^= fmix32(H ^ k_i)
+    mod 2^|L|.  Each round undoes itself, so the pass is a bijection of
+    [0, 2^bits) whatever the round function."""
     h_hi, h_lo, m_hi, m_lo = _feistel_params(n)
-    rk = splitmix64_stream(key, FEISTEL_ROUNDS)
+    rk = feistel_round_keys(key)
     H, L = x >> h_lo, x & m_lo
     for i in range(FEISTEL_ROUNDS):
         if i % 2 == 0:
-            H ^= splitmix64_mix(L ^ rk[i]) & m_hi
+            H ^= murmur3_fmix32(L ^ rk[i]) & m_hi
         else:
-            L ^= splitmix64_mix(H ^ rk[i]) & m_lo
+            L ^= murmur3_fmix32(H ^ rk[i]) & m_lo
     return (H << h_lo) | L
 
 
@@ -389,28 +408,28 @@ def keyed_perm(j: int, key: int, n: int) -> int:
 
 def keyed_perm_all(key: int, n: int) -> np.ndarray:
     """π_key(0..n-1) for every index, numpy-vectorised version of keyed_perm
-    (same arithmetic on uint64 lanes; wrapping multiplication mod 2^64)."""
+    (same arithmetic on uint32 halves; wrapping multiplication mod 2^32)."""
     if n <= 1:
         return np.arange(n, dtype=np.int64)
     h_hi, h_lo, m_hi, m_lo = _feistel_params(n)
-    rk = [np.uint64(k) for k in splitmix64_stream(key, FEISTEL_ROUNDS)]
-    mh, ml, hl = np.uint64(m_hi), np.uint64(m_lo), np.uint64(h_lo)
+    rk = [np.uint32(k) for k in feistel_round_keys(key)]
+    mh, ml, hl = np.uint32(m_hi), np.uint32(m_lo), np.uint64(h_lo)
 
-    def mix(z):
-        z = z ^ (z >> np.uint64(30))
-        z = z * np.uint64(0xBF58476D1CE4E5B9)
-        z = z ^ (z >> np.uint64(27))
-        z = z * np.uint64(0x94D049BB133111EB)
-        return z ^ (z >> np.uint64(31))
+    def fmix(h):
+        h = h ^ (h >> np.uint32(16))
+        h = h * np.uint32(0x85EBCA6B)
+        h = h ^ (h >> np.uint32(13))
+        h = h * np.uint32(0xC2B2AE35)
+        return h ^ (h >> np.uint32(16))
 
     def enc(x):
-        H, L = x >> hl, x & ml
+        H, L = (x >> hl).astype(np.uint32), (x & np.uint64(m_lo)).astype(np.uint32)
         for i in range(FEISTEL_ROUNDS):
             if i % 2 == 0:
-                H = H ^ (mix(L ^ rk[i]) & mh)
+                H = H ^ (fmix(L ^ rk[i]) & mh)
             else:
-                L = L ^ (mix(H ^ rk[i]) & ml)
-        return (H << hl) | L
+                L = L ^ (fmix(H ^ rk[i]) & ml)
+        return (H.astype(np.uint64) << hl) | L.astype(np.uint64)
 
     with np.errstate(over="ignore"):
         y = enc(np.arange(n, dtype=np.uint64))

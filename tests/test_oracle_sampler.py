@@ -14,6 +14,30 @@ def test_splitmix64_known_answers():
     assert oracle.splitmix64_stream(0, 3) == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
 
 
+def test_fmix32_known_answers():
+    """MurmurHash3_x86_32 of the empty key is fmix32(seed): the published
+    outputs for seeds 1 and 0xFFFFFFFF are 0x514E28B7 and 0x81F16F39; 0 is a
+    fixed point."""
+    assert oracle.murmur3_fmix32(1) == 0x514E28B7
+    assert oracle.murmur3_fmix32(0xFFFFFFFF) == 0x81F16F39
+    assert oracle.murmur3_fmix32(0) == 0
+
+
+def test_round_keys_are_high_halves():
+    """Round keys: the high 32 bits of the SplitMix64 outputs from state 0
+    (published values above)."""
+    assert oracle.feistel_round_keys(0)[:3] == [0xE220A839, 0x6E789E6A, 0x06C45D18]
+
+
+def test_vectorised_perm_matches_scalar_definition():
+    """keyed_perm_all and keyed_perm (scalar Python ints) agree for a domain
+    with unequal halves (21 bits) on a sample of indices."""
+    n = 1_281_167
+    p = oracle.keyed_perm_all(9, n)
+    for j in list(range(50)) + list(range(n - 50, n)) + [123_457, 654_321]:
+        assert p[j] == oracle.keyed_perm(j, 9, n)
+
+
 def test_feistel_is_a_bijection_on_its_domain():
     """Every encryption pass permutes [0, 2^bits), bits = ceil(log2 n), for
     odd and even widths up to 12 bits and several keys (brute force), and the
