@@ -44,7 +44,10 @@ CAP_BYTES = 25 * MiB
 METRIC = "bucket allreduce-mean GB/s (HBM bytes moved) & % of HBM roofline, 1×GB300"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 10 ** 6
-SAMPLER_LANE_INSTR_PER_INDEX = 241.6   # ncu, 1,281,167 items over 8 ranks (profiles/sampler_imagenet.md)
+# Warp instructions one sampler launch issues on the ImageNet-size workload (1,281,168 output
+# slots), by pipe, from an ncu capture of this launch.  The integer ALU and the FMA-heavy
+# pipe each take 2 warp instructions per SM cycle; the four schedulers issue 4 per SM cycle.
+SAMPLER_WARP_INST = {"alu": 2_706_042, "fmaheavy": 2_147_028, "all": 6_238_443}
 
 
 def parse_args():
@@ -602,11 +605,11 @@ def bench_rows(g, torch, dev, peak, peak_kind):
     n, N = workloads.SAMPLER_N_ITEMS, workloads.SAMPLER_REPLICAS
     out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
     ms = _time_launches(torch, lambda: g.dist_sampler_indices(n, N, -1, 0, 1, True, False, out), 100, side)
-    # ALU roofline: lane-instruction issue peak (152 SMs x 4 schedulers x 32 lanes x 2.07 GHz) over the
-    # lane-instructions one index needs on this workload (ncu, profiles/sampler_imagenet.md)
-    lane_issue_peak = 152 * 4 * 32 * 2.07e9
+    # Integer-pipe roofline: the launch's measured instruction stream at full issue -- the slowest of
+    # ALU pipe (2 / SM cycle), FMA-heavy pipe (2 / SM cycle) and issue (4 / SM cycle), 152 SMs, 2.07 GHz
+    sm_cycles = max(SAMPLER_WARP_INST["alu"] / 2, SAMPLER_WARP_INST["fmaheavy"] / 2, SAMPLER_WARP_INST["all"] / 4) / 152
     idx_per_s = out.numel() / (ms * 1e-3)
-    peak_idx = lane_issue_peak / SAMPLER_LANE_INSTR_PER_INDEX
+    peak_idx = out.numel() / (sm_cycles / 2.07e9)
     rows["sampler_imagenet"] = {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
                                 "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
                                 "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",

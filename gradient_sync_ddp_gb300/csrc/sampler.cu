@@ -29,27 +29,28 @@ namespace {
 constexpr uint64_t kGamma = 0x9E3779B97F4A7C15ull;
 constexpr int kRounds = 4;
 constexpr int kWalkCap = 4096;
-constexpr int kBlocksPerSm = 2;                    // target CTAs per SM (fewer if occupancy caps it)
-constexpr int kWalks = 1;                          // independent walks per lane
+constexpr int kBlocksPerSm = 3;                    // target CTAs per SM (fewer if occupancy caps it)
 constexpr int64_t kMinItemsPerWarp = 64;
 constexpr int kWarpsPerBlock = kThreads / 32;
 
 struct SamplerParams {
     int64_t* out;
     int32_t* status;
-    uint32_t rk[kRounds];
-    uint64_t n;          // items
-    uint32_t mask_hi;    // 2^h_hi - 1
-    uint32_t mask_lo;    // 2^h_lo - 1
-    int64_t ns;          // num_samples
-    int64_t count;       // outputs to write
-    int64_t per_warp;    // slots per pool
-    int64_t pools;       // ceil(count / per_warp)
-    FastDiv ns_div;      // division by ns, valid when small != 0
-    int32_t small;       // count < 2^31
-    int32_t N;           // replicas
-    int32_t rank;        // -1: all ranks, rank-major
-    int32_t h_lo;        // width of the low half
+    uint32_t rk[kRounds];   // round keys
+    uint32_t rkx[kRounds];  // k ^ (k >> 16): the key after fmix32's first xor-shift
+    uint32_t sh16;          // 2^16 and 2^19: __umulhi(h, 2^(32-s)) == h >> s, which
+    uint32_t sh19;          //   issues on the multiply pipe instead of the integer ALU
+    uint32_t p2lo;          // 2^h_lo
+    uint32_t mask_hi;       // 2^h_hi - 1
+    uint32_t mask_lo;       // 2^h_lo - 1
+    int32_t h_lo;           // width of the low half
+    uint64_t n;             // items
+    int64_t ns;             // num_samples (length of a rank's row)
+    int64_t per_warp;       // slots per pool; pools never cross a row
+    int64_t pools_per_row;  // ceil(ns / per_warp)
+    int64_t pools;          // rows * pools_per_row
+    int32_t N;              // replicas
+    int32_t rank;           // -1: all ranks, rank-major rows
     int32_t shuffle;
 };
 
@@ -61,114 +62,100 @@ uint64_t splitmix64_mix(uint64_t z) {
     return z ^ (z >> 31);
 }
 
-__device__ __forceinline__ uint32_t fmix32(uint32_t h) {
-    h ^= h >> 16;
+// fmix32(x ^ k), the MurmurHash3 32-bit finalizer, with its shifts written
+// as multiply-highs.  NARROW: x < 2^16, so x >> 16 == 0 and the first
+// xor-shift of x ^ k is x ^ (k ^ (k >> 16)) (shifts distribute over xor).
+template <bool NARROW>
+__device__ __forceinline__ uint32_t round_fn(uint32_t x, int i, const SamplerParams& a) {
+    uint32_t h;
+    if constexpr (NARROW) {
+        h = x ^ a.rkx[i];
+    } else {
+        h = x ^ a.rk[i];
+        h ^= __umulhi(h, a.sh16);
+    }
     h *= 0x85EBCA6Bu;
-    h ^= h >> 13;
+    h ^= __umulhi(h, a.sh19);
     h *= 0xC2B2AE35u;
-    return h ^ (h >> 16);
+    return h ^ __umulhi(h, a.sh16);
 }
 
-// x = (H, L) with H the high ceil(bits/2) bits and L the low floor(bits/2)
-// bits; even rounds H ^= fmix32(L ^ k_i) mod 2^|H|, odd rounds L ^= fmix32(H
-// ^ k_i) mod 2^|L|.  Every round undoes itself, so the pass is a bijection.
-template <typename U>
-__device__ __forceinline__ U encrypt(U x, const SamplerParams& a) {
-    uint32_t H = static_cast<uint32_t>(x >> a.h_lo), L = static_cast<uint32_t>(x) & a.mask_lo;
+// One pass of the network on x = (H, L), H the high ceil(bits/2) bits and L
+// the low floor(bits/2) bits: even rounds H ^= fmix32(L ^ k_i) mod 2^|H|,
+// odd rounds L ^= fmix32(H ^ k_i) mod 2^|L|.  Every round undoes itself, so
+// the pass is a bijection.
+template <bool NARROW>
+__device__ __forceinline__ void encrypt(uint32_t& H, uint32_t& L, const SamplerParams& a) {
 #pragma unroll
     for (int i = 0; i < kRounds; ++i) {
-        if (i % 2 == 0) H ^= fmix32(L ^ a.rk[i]) & a.mask_hi;
-        else L ^= fmix32(H ^ a.rk[i]) & a.mask_lo;
+        if (i % 2 == 0) H ^= round_fn<NARROW>(L, i, a) & a.mask_hi;
+        else L ^= round_fn<NARROW>(H, i, a) & a.mask_lo;
     }
-    return (static_cast<U>(H) << a.h_lo) | L;
 }
 
-// Output slot i -> unshuffled index: slot (r, s) of the rank-major output
-// holds padded-list position r + s*N; padding repeats the head.  U = uint32_t
-// is used only when n <= 2^31 and count < 2^31; then every position is below
-// total < n + N < 2^32 and the whole computation fits 32 bits.
+// Padded-list position -> unshuffled index: padding repeats the head.
 template <typename U>
-__device__ __forceinline__ U base_index(int64_t i, const SamplerParams& a) {
-    U r, s;
-    if (a.rank >= 0) {
-        r = static_cast<U>(a.rank);
-        s = static_cast<U>(i);
-    } else {
-        if constexpr (sizeof(U) == 4) r = fdiv(static_cast<uint32_t>(i), a.ns_div);
-        else r = static_cast<U>(i / a.ns);
-        s = static_cast<U>(i) - r * static_cast<U>(a.ns);
-    }
-    const U pos = r + s * static_cast<U>(a.N);
-    const U n = static_cast<U>(a.n);
+__device__ __forceinline__ U wrap(U pos, U n) {
     if (pos < n) return pos;
     return pos - n < n ? pos - n : pos % n;    // pos >= 2n only when N > n
 }
 
-// Warps take pools of per_warp consecutive output slots (grid-stride over
-// pools; the host sizes pools so that the grid is kBlocksPerSm CTAs on every
-// SM).  Each lane carries kWalks independent cycle walks, so a warp acts as
-// 32*kWalks virtual lanes and two dependency chains interleave.  Walk
-// lengths are geometric: instead of idling until the slowest walk of the
-// warp has finished, a virtual lane whose walk ends writes its index and
+// A pool is per_warp consecutive slots s0 .. s0+len-1 of one rank's row r;
+// slot s holds padded-list position r + s*N.  Warps take pools grid-stride;
+// the host sizes pools so that the grid is kBlocksPerSm CTAs on every SM.
+// Cycle-walk lengths are geometric: instead of idling until the slowest
+// lane of the warp has finished, a lane whose walk ends writes its index and
 // takes the pool's next unclaimed slot (ballot + prefix count), so every
-// iteration is one encryption per virtual lane until the pool runs dry.  The
-// body is written with selects rather than branches; lanes without a slot
-// compute on a clamped copy and store nothing.
+// iteration is one encryption per lane until the pool runs dry.  The body
+// uses selects, not branches; a lane without a slot computes on a clamped
+// copy and stores nothing.  U is uint32_t when n <= 2^31: then every
+// position is below total < n + N < 2^32 and both halves below 2^16.
 template <typename U>
 __global__ void __launch_bounds__(kThreads) sampler_kernel(const __grid_constant__ SamplerParams a) {
+    constexpr bool kNarrow = sizeof(U) == 4;
     const int lane = threadIdx.x & 31;
     const unsigned lanes_below = (1u << lane) - 1u;
     const U n = static_cast<U>(a.n);
+    const U N = static_cast<U>(a.N);
     const int64_t warps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
     for (int64_t pool = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) / 32; pool < a.pools;
          pool += warps) {
-        const int64_t begin = pool * a.per_warp;
-        const int32_t len = static_cast<int32_t>(min(a.per_warp, a.count - begin));
-        int64_t* out = a.out + begin;
+        const int64_t row = pool / a.pools_per_row;
+        const int64_t s0 = (pool - row * a.pools_per_row) * a.per_warp;
+        const int32_t len = static_cast<int32_t>(min(a.per_warp, a.ns - s0));
+        const int64_t r = a.rank >= 0 ? a.rank : row;
+        int64_t* out = a.out + (a.rank >= 0 ? 0 : row * a.ns) + s0;
+        const U pos0 = static_cast<U>(r) + static_cast<U>(s0) * N;
         if (!(a.shuffle && a.n > 1)) {
-            for (int32_t o = lane; o < len; o += 32) out[o] = static_cast<int64_t>(base_index<U>(begin + o, a));
+            for (int32_t o = lane; o < len; o += 32) out[o] = static_cast<int64_t>(wrap<U>(pos0 + o * N, n));
             continue;
         }
-        int32_t off[kWalks];                       // slot of each walk, relative to begin
-        U y[kWalks];
-        int32_t steps[kWalks];                     // encryptions applied to y
-        bool live[kWalks];
-#pragma unroll
-        for (int v = 0; v < kWalks; ++v) {
-            off[v] = v * 32 + lane;
-            live[v] = off[v] < len;
-            y[v] = base_index<U>(begin + min(off[v], len - 1), a);
-            steps[v] = 0;
-        }
-        int32_t next = 32 * kWalks;                // first unclaimed slot of the pool
-        while (true) {
-            bool any_live = false;
-#pragma unroll
-            for (int v = 0; v < kWalks; ++v) any_live |= live[v];
-            if (!__any_sync(0xffffffffu, any_live)) break;
-            bool done[kWalks];
-            int capped = 0;
-#pragma unroll
-            for (int v = 0; v < kWalks; ++v) {
-                y[v] = encrypt<U>(y[v], a);
-                ++steps[v];
-                const bool hit = y[v] < n;
-                done[v] = live[v] && (hit || steps[v] >= kWalkCap);
-                if (done[v]) out[off[v]] = hit ? static_cast<int64_t>(y[v]) : int64_t(-1);
-                capped += (done[v] && !hit) ? 1 : 0;
+        int32_t off = lane;                        // this lane's slot in the pool
+        U b = wrap<U>(pos0 + static_cast<U>(min(off, len - 1)) * N, n);
+        uint32_t H = static_cast<uint32_t>(b >> a.h_lo), L = static_cast<uint32_t>(b) & a.mask_lo;
+        int32_t steps = 0;                         // encryptions since the walk began
+        int32_t next = 32;                         // first unclaimed slot of the pool
+        while (__any_sync(0xffffffffu, off < len)) {
+            encrypt<kNarrow>(H, L, a);
+            const U y = static_cast<U>(H) * a.p2lo + L;
+            ++steps;
+            const bool live = off < len;
+            const bool hit = y < n;
+            if (live && hit) out[off] = static_cast<int64_t>(y);
+            const bool done = live && (hit || steps >= kWalkCap);
+            if (done && !hit) {                    // walk bound reached: never observed
+                out[off] = -1;
+                if (a.status) atomicAdd(a.status, 1);
             }
-            if (capped && a.status) atomicAdd(a.status, capped);   // walk bound reached: never observed
-#pragma unroll
-            for (int v = 0; v < kWalks; ++v) {
-                const unsigned fin = __ballot_sync(0xffffffffu, done[v]);
-                const int32_t o = next + __popc(fin & lanes_below);
-                next += __popc(fin);
-                const U yb = base_index<U>(begin + min(o, len - 1), a);
-                off[v] = done[v] ? o : off[v];
-                live[v] = done[v] ? o < len : live[v];
-                y[v] = done[v] ? yb : y[v];
-                steps[v] = done[v] ? 0 : steps[v];
-            }
+            const unsigned fin = __ballot_sync(0xffffffffu, done);
+            const int32_t o = next + __popc(fin & lanes_below);
+            next += __popc(fin);
+            b = wrap<U>(pos0 + static_cast<U>(min(o, len - 1)) * N, n);
+            const uint32_t Hn = static_cast<uint32_t>(b >> a.h_lo), Ln = static_cast<uint32_t>(b) & a.mask_lo;
+            off = done ? o : off;
+            H = done ? Hn : H;
+            L = done ? Ln : L;
+            steps = done ? 0 : steps;
         }
     }
 }
@@ -216,23 +203,24 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     for (int i = 0; i < kRounds; ++i) {           // SplitMix64 stream from `key`
         state += kGamma;
         p.rk[i] = static_cast<uint32_t>(splitmix64_mix(state) >> 32);
+        p.rkx[i] = p.rk[i] ^ (p.rk[i] >> 16);
     }
+    p.sh16 = 1u << 16;
+    p.sh19 = 1u << 19;
     const uint64_t n = static_cast<uint64_t>(n_items);
     int bits = 1;
     while (bits < 62 && (uint64_t(1) << bits) < n) ++bits;   // smallest bits >= 1 with 2^bits >= n
     p.h_lo = bits / 2;                                        // both halves <= 31 bits
-    p.mask_lo = static_cast<uint32_t>((uint64_t(1) << p.h_lo) - 1);
+    p.p2lo = 1u << p.h_lo;
+    p.mask_lo = p.p2lo - 1u;
     p.mask_hi = static_cast<uint32_t>((uint64_t(1) << (bits - p.h_lo)) - 1);
     p.n = n;
     p.ns = ns;
-    p.count = count;
-    p.small = count < (int64_t(1) << 31) ? 1 : 0;
-    if (p.small) p.ns_div = make_fastdiv(static_cast<uint32_t>(ns));
     p.N = n_replicas;
     p.rank = rank;
     p.shuffle = shuffle;
 
-    const bool narrow = n <= (uint64_t(1) << 31) && p.small;
+    const bool narrow = n <= (uint64_t(1) << 31);
     const void* kernel = narrow ? reinterpret_cast<const void*>(sampler_kernel<uint32_t>)
                                 : reinterpret_cast<const void*>(sampler_kernel<uint64_t>);
     DeviceInfo dev;
@@ -245,8 +233,11 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     p.per_warp = (count + target_warps - 1) / target_warps;
     if (p.per_warp < kMinItemsPerWarp) p.per_warp = kMinItemsPerWarp;
     if (p.per_warp > (int64_t(1) << 30)) p.per_warp = int64_t(1) << 30;   // pool offsets stay int32
-    p.pools = (count + p.per_warp - 1) / p.per_warp;
-    const int grid = static_cast<int>((p.pools + kWarpsPerBlock - 1) / kWarpsPerBlock);   // <= target blocks
+    p.pools_per_row = (ns + p.per_warp - 1) / p.per_warp;
+    p.pools = (rank >= 0 ? 1 : n_replicas) * p.pools_per_row;
+    const int64_t need = (p.pools + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const int64_t wave = static_cast<int64_t>(dev.sm_count) * per_sm;
+    const int grid = static_cast<int>(need < wave ? need : wave);
     // plain launch: the status word's memset just before must complete first
     if (narrow) sampler_kernel<uint32_t><<<grid, kThreads, 0, s>>>(p);
     else sampler_kernel<uint64_t><<<grid, kThreads, 0, s>>>(p);

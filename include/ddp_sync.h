@@ -416,9 +416,10 @@ int64_t dist_sampler_num_samples(int64_t n_items, int32_t n_replicas, int32_t dr
  * r, r+N, r+2N, ...  The shuffle is a permutation keyed by seed+epoch so
  * every rank agrees without communication: a 4-round Feistel network on
  * ceil(log2 n) bits (a high half of ceil(bits/2) bits and a low half of
- * floor(bits/2) bits, updated alternately) whose round keys are the first
- * four SplitMix64 outputs from state seed+epoch and whose round function is
- * the SplitMix64 output mix, with cycle walking into [0, n).
+ * floor(bits/2) bits, updated alternately) whose round keys are the high 32
+ * bits of the first four SplitMix64 outputs from state seed+epoch and whose
+ * round function is the MurmurHash3 32-bit finalizer of (half ^ key),
+ * truncated to the other half's width, with cycle walking into [0, n).
  *
  *   n_items        n >= 0 (< 2^62)
  *   n_replicas     N >= 1
