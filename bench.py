@@ -47,6 +47,8 @@ L2_BYTES = 129 * 10 ** 6
 # Warp instructions one sampler launch issues on the ImageNet-size workload (1,281,168 output
 # slots), by pipe, from an ncu capture of this launch.  The integer ALU and the FMA-heavy
 # pipe each take 2 warp instructions per SM cycle; the four schedulers issue 4 per SM cycle.
+SYNCBN_CALLS = 10      # calls captured per graph in the SyncBN rows
+SAMPLER_CALLS = 20     # calls (epochs 1..20) captured per graph in the sampler row
 SAMPLER_WARP_INST = {"alu": 2_706_042, "fmaheavy": 2_147_028, "all": 6_238_443}
 
 
@@ -593,18 +595,22 @@ def bench_rows(g, torch, dev, peak, peak_kind):
         ws = torch.empty(g.syncbn_workspace_bytes(N_REPLICAS, B, C, H, W), dtype=torch.uint8, device=dev)
         mean = torch.empty(C, device=dev)
         inv = torch.empty(C, device=dev)
-        ms = _time_launches(torch, lambda: g.syncbn_merge_apply(xs, ys, mean, inv, ws), 30, side)
+        # SYNCBN_CALLS back-to-back calls per graph replay (as consecutive BN layers sit in a captured
+        # step), so the figure is device time per call, not one graph launch's latency per call
+        ms = _time_launches(torch, lambda: [g.syncbn_merge_apply(xs, ys, mean, inv, ws) for _ in range(SYNCBN_CALLS)],
+                            10, side) / SYNCBN_CALLS
         nbytes = 6 * N_REPLICAS * B * C * H * W
         rows[f"syncbn_{C}x{H}x{W}"] = {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
                                        "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-                                       "launches": 3,
+                                       "launches": 3, "calls_per_graph": SYNCBN_CALLS,
                                        "note": "inputs smaller than L2" if nbytes / 3 < L2_BYTES else ""}
         del xs, ys
 
     # sampler
     n, N = workloads.SAMPLER_N_ITEMS, workloads.SAMPLER_REPLICAS
     out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
-    ms = _time_launches(torch, lambda: g.dist_sampler_indices(n, N, -1, 0, 1, True, False, out), 100, side)
+    ms = _time_launches(torch, lambda: [g.dist_sampler_indices(n, N, -1, 0, 1 + e, True, False, out)
+                                        for e in range(SAMPLER_CALLS)], 10, side) / SAMPLER_CALLS
     # Integer-pipe roofline: the launch's measured instruction stream at full issue -- the slowest of
     # ALU pipe (2 / SM cycle), FMA-heavy pipe (2 / SM cycle) and issue (4 / SM cycle), 152 SMs, 2.07 GHz
     sm_cycles = max(SAMPLER_WARP_INST["alu"] / 2, SAMPLER_WARP_INST["fmaheavy"] / 2, SAMPLER_WARP_INST["all"] / 4) / 152
@@ -614,7 +620,7 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                                 "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
                                 "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
                                 "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
-                                "launches": 1}
+                                "launches": 1, "calls_per_graph": SAMPLER_CALLS}
     # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point)
     sweep = []
     for size in (4 << 20, 64 << 20, 1 << 30):

@@ -16,13 +16,12 @@
 //        plane kernel — H*W a multiple of the 16-byte vector (56x56, 28x28):
 //          CTA (c, s) streams its planes with 16-byte loads, a warp at a
 //          time over 64-vector chunks of one plane.
-//        segment kernel — unaligned planes at least one vector long (7x7,
-//          14x14, 3x3): a CTA owns G consecutive channels (G*H*W about 2K
-//          elements) and a slice of the samples; for one sample those G
-//          channels are one contiguous run, read as the aligned 16-byte
-//          vectors that cover it.  A vector spans at most two channels, so a
-//          thread reduces it to two (Σd, Σd²) segments in shared memory, and
-//          one thread per (sample, channel) then adds its channel's segments.
+//        bulk-staged kernel — unaligned planes at least one vector long
+//          (7x7, 14x14, 3x3): a CTA owns G consecutive channels (G*H*W about
+//          2K elements) and a slice of the samples; for one sample those G
+//          channels are one contiguous run, copied into shared memory by one
+//          bulk asynchronous copy, and each lane sums a contiguous range of
+//          one channel's plane there.
 //        staged group kernel — planes shorter than a vector (1x1, 2x2):
 //          runs are copied to shared memory and reduced per channel there.
 //        element kernel — unaligned planes too long to stage (111x111).
@@ -46,7 +45,9 @@
 //      x·scale + (β − mean·scale) would lose it).
 // Traffic: x is read twice and y written once (2+2+2 bytes per bf16 element).
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "host_common.h"
@@ -72,10 +73,14 @@ struct BnParams {
     FastDiv div_batch;  // batch
     FastDiv div_hw;     // H*W
     FastDiv div_c;      // C
+    FastDiv div_s;      // S, valid when ps_small
+    int32_t ps_small;   // n*batch*S < 2^31: slice bounds in 32-bit arithmetic
     int32_t n, batch, C, HW, S;
     int32_t G;          // group kernel: channels per CTA (power of two)
     int32_t R;          // group kernel: runs staged per tile
     int32_t slot_bytes; // group kernel: shared bytes per staged run
+    int32_t tc_log2;    // bulk kernel: log2 of the lanes per channel (32/G for G < 32, else 0)
+    uint64_t buf_fl;    // bulk kernel: replica bytes rounded down to 16 (copies stop there)
     float eps;
 };
 
@@ -83,6 +88,18 @@ template <bool BF16>
 __device__ __forceinline__ float shared_elem(const unsigned char* p, int e) {
     if constexpr (BF16) return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short*>(p)[e]) << 16);
     else return reinterpret_cast<const float*>(p)[e];
+}
+
+// Samples [p0, p1) of slice s: p_k = floor(P*k/S) with P = n*batch.
+__device__ __forceinline__ void slice_bounds(const BnParams& a, int s, int& p0, int& p1) {
+    const int P = a.n * a.batch;
+    if (a.ps_small) {
+        p0 = static_cast<int>(fdiv(static_cast<uint32_t>(P * s), a.div_s));
+        p1 = static_cast<int>(fdiv(static_cast<uint32_t>(P * (s + 1)), a.div_s));
+    } else {
+        p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
+        p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
+    }
 }
 
 // Group kernel, grid (ceil(C/G), S).
@@ -96,9 +113,8 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
     const int Tc = kThreads / a.G;                // threads per channel
     const int cl = threadIdx.x / Tc, k = threadIdx.x - cl * Tc;
     const bool active = cl < Gc;
-    const int P = a.n * a.batch;
-    const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
-    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
+    int p0, p1;
+    slice_bounds(a, s, p0, p1);
     const uint64_t run_bytes = static_cast<uint64_t>(Gc) * a.HW * ESZ;
     const uint32_t vslot = static_cast<uint32_t>(a.slot_bytes / 16);
     pdl_enter();
@@ -168,163 +184,264 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
     }
 }
 
-// Segment kernel, grid (ceil(C/G), S), for H*W >= the vector width W and not
-// a multiple of it (7x7, 14x14, 3x3, ...).  Runs (one sample's G channels)
-// are read as the 16-byte vectors of the aligned grid that covers them, so a
-// vector holds elements of at most two channels of the group (or of the
-// neighbouring groups, which are masked out).  Phase A: each thread turns
-// one vector into (Σd, Σd²) of its first channel and of the next one and
-// stores them in shared memory.  Phase B: thread (run j, channel cl, part k)
-// adds up the segments of channel cl's vectors.  Interior vectors take a
-// mask-free path; only a run's first and last vectors are masked, and the
-// last one is read element by element where it would extend past the run,
-// so no access leaves the replica buffer.
-constexpr int kMaxRuns = 128;
+// Bulk-staged kernel, grid (ceil(C/G), S), for H*W >= the vector width W
+// and not a multiple of it (7x7, 14x14, 3x3, ...).  A run (one sample's G
+// consecutive channels) is contiguous in memory; the 16-byte aligned blocks
+// that cover it are copied into shared memory by one bulk asynchronous copy
+// (the copy engine moves them without registers; completion is counted on
+// an mbarrier).  Only where the replica buffer ends inside a block is the
+// run's end read with plain loads.  A tile is up to kBulkRuns runs; two
+// tile buffers alternate, so the copy of tile t+2 runs while tile t+1 is
+// summed.  Warp w sums run w of the tile; within a run, lane l owns a
+// contiguous range of one channel's plane (G >= 32: whole planes of channels
+// l, l+32, ...; G < 32: 32/G lanes split each plane), so every element it
+// reads belongs to its channel and needs no mask.  Each wait for a copy is
+// bounded (about a second of globaltimer): on expiry the CTA writes NaN
+// partials for its channels, which makes the statistics NaN, instead of
+// waiting on.
+constexpr int kBulkRuns = kThreads / 32;   // runs per tile: one per warp
+constexpr int kBulkBufMax = 32768;        // bytes per tile buffer at most
+constexpr uint64_t kCopyWaitNs = 1000000000ull;
 
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One poll of the barrier's phase; the thread may be suspended for up to
+// kPollSuspendNs while the phase is incomplete.
+constexpr uint32_t kPollSuspendNs = 100000;
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kPollSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Sum (x - K) and (x - K)^2 over `count` elements starting at byte `byte0`
+// of the shared buffer `buf` (element aligned; 32-bit words read).
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads) bn_stats_segment_kernel(const __grid_constant__ BnParams a) {
+__device__ __forceinline__ void sum_range(const unsigned char* buf, uint32_t byte0, uint32_t count, float K,
+                                          float& acc_s, float& acc_q) {
+    float s0 = 0.0f, s1 = 0.0f, q0 = 0.0f, q1 = 0.0f;
+    if constexpr (BF16) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(buf);
+        uint32_t h = byte0 >> 1;
+        const uint32_t hend = h + count;
+        if ((h & 1u) && h < hend) {                          // odd start: high half of a word
+            const float d = __fsub_rn(__uint_as_float(w[h >> 1] & 0xFFFF0000u), K);
+            s0 += d;
+            q0 = fmaf(d, d, q0);
+            ++h;
+        }
+        for (; h + 8 <= hend; h += 8) {
+            uint32_t v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] = w[(h >> 1) + i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float dl = __fsub_rn(__uint_as_float(v[i] << 16), K);
+                const float dh = __fsub_rn(__uint_as_float(v[i] & 0xFFFF0000u), K);
+                s0 += dl;
+                q0 = fmaf(dl, dl, q0);
+                s1 += dh;
+                q1 = fmaf(dh, dh, q1);
+            }
+        }
+        for (; h + 2 <= hend; h += 2) {
+            const uint32_t v = w[h >> 1];
+            const float dl = __fsub_rn(__uint_as_float(v << 16), K);
+            const float dh = __fsub_rn(__uint_as_float(v & 0xFFFF0000u), K);
+            s0 += dl;
+            q0 = fmaf(dl, dl, q0);
+            s1 += dh;
+            q1 = fmaf(dh, dh, q1);
+        }
+        if (h < hend) {                                      // last element: low half of a word
+            const float d = __fsub_rn(__uint_as_float(w[h >> 1] << 16), K);
+            s0 += d;
+            q0 = fmaf(d, d, q0);
+        }
+    } else {
+        const float* f = reinterpret_cast<const float*>(buf) + (byte0 >> 2);
+        uint32_t i = 0;
+        for (; i + 4 <= count; i += 4) {
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+                const float da = __fsub_rn(f[i + u], K), db = __fsub_rn(f[i + u + 1], K);
+                s0 += da;
+                q0 = fmaf(da, da, q0);
+                s1 += db;
+                q1 = fmaf(db, db, q1);
+            }
+        }
+        for (; i < count; ++i) {
+            const float d = __fsub_rn(f[i], K);
+            s0 += d;
+            q0 = fmaf(d, d, q0);
+        }
+    }
+    acc_s += s0 + s1;
+    acc_q += q0 + q1;
+}
+
+template <bool BF16, int CPL>
+__global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_constant__ BnParams a) {
     constexpr int ESZ = BF16 ? 2 : 4;
-    constexpr int W = 16 / ESZ;
-    __shared__ float4 seg[kStageBytes / 16];
-    __shared__ float Ks[kThreads + 1];
-    __shared__ const char* rbase[kMaxRuns];
-    __shared__ int32_t rpre[kMaxRuns];
-    __shared__ float red[2][kThreads];
+    constexpr int kWarps = kThreads / 32;
+    extern __shared__ __align__(128) unsigned char smem[];   // two tile buffers of R * slot_bytes
+    __shared__ uint64_t bar[2];
     const int c0 = blockIdx.x * a.G, s = blockIdx.y;
     const int Gc = min(a.G, a.C - c0);
     const int HW = a.HW;
-    const int P = a.n * a.batch;
-    const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
-    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
-    const uint32_t vslot = static_cast<uint32_t>(a.slot_bytes / 16);   // vectors per run (upper bound)
-    const int32_t run_elems = Gc * HW;
-    // phase-B role: pair (j, cl) and part k of Tk
-    const int Tk = kThreads / (a.R * a.G);
-    const int pair = threadIdx.x / Tk, k = threadIdx.x - pair * Tk;
-    const int jb = pair / a.G, cl = pair - jb * a.G;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int p0, p1;
+    slice_bounds(a, s, p0, p1);
+    const int R = a.R;                                       // runs per tile
+    const int ntiles = (p1 - p0 + R - 1) / R;
+    const uint32_t buf_bytes = static_cast<uint32_t>(R) * a.slot_bytes;
+    const uint32_t run_bytes = static_cast<uint32_t>(Gc) * HW * ESZ;
+    // this lane's channels (CPL = G/32 of them when G >= 32) and element range within a plane;
+    // Tc = 2^tc_log2 lanes per channel (G < 32), so the splits are shifts
+    const int Tc = 1 << a.tc_log2;
+    const int part = lane & (Tc - 1);
+    const uint32_t e_lo = (static_cast<uint32_t>(HW) * part) >> a.tc_log2;
+    const uint32_t e_hi = (static_cast<uint32_t>(HW) * (part + 1)) >> a.tc_log2;
+    int cl[CPL];
+    float K[CPL], acc_s[CPL], acc_q[CPL];
     pdl_enter();
-    if (threadIdx.x < Gc) Ks[threadIdx.x] = load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + threadIdx.x) * HW);
-    if (threadIdx.x == 0) Ks[Gc] = 0.0f;      // read only for elements past the group, which are masked
-
-    float acc_s = 0.0f, acc_q = 0.0f;
-    for (int t0 = p0; t0 < p1; t0 += a.R) {
-        const int nr = min(a.R, p1 - t0);
-        if (threadIdx.x < nr) {                       // per-run base (aligned down) and misalignment
-            const uint32_t pl = static_cast<uint32_t>(t0 + threadIdx.x);
-            const uint32_t r = fdiv(pl, a.div_batch);
-            const uint32_t b = pl - r * static_cast<uint32_t>(a.batch);
-            const uint64_t first = (static_cast<uint64_t>(b) * a.C + c0) * HW;
-            const uint32_t pre = static_cast<uint32_t>(first % W);
-            rbase[threadIdx.x] = static_cast<const char*>(a.x[r]) + (first - pre) * ESZ;
-            rpre[threadIdx.x] = static_cast<int32_t>(pre);
-        }
-        __syncthreads();
-        // phase A: four vectors per thread per iteration, all loads issued before the arithmetic
-        const uint32_t total = static_cast<uint32_t>(nr) * vslot;
-        for (uint32_t t0 = threadIdx.x; t0 < total; t0 += 4 * kThreads) {
-            uint4 raw[4];
-            int32_t es[4];
-            uint32_t slot[4];
-            bool interior[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const uint32_t t = t0 + u * kThreads;
-                es[u] = INT32_MAX;
-                interior[u] = false;
-                if (t < total) {
-                    const uint32_t j = fdiv(t, a.div_unit);
-                    const uint32_t v = t - j * vslot;
-                    slot[u] = j * vslot + v;
-                    es[u] = static_cast<int32_t>(v * W) - rpre[j];
-                    const char* ptr = rbase[j] + 16ull * v;
-                    interior[u] = es[u] >= 0 && es[u] + W <= run_elems;
-                    if (interior[u]) raw[u] = ld16<true>(ptr);
-                    else if (es[u] < run_elems) {                         // first or last vector of the run
-                        float xe[W];
-                        if (es[u] + W <= run_elems) {
-                            const uint4 r4 = ld16<true>(ptr);
-#pragma unroll
-                            for (int q = 0; q < W; ++q) xe[q] = vec_elem<BF16>(r4, q);
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < W; ++q)
-                                xe[q] = (es[u] + q < run_elems) ? load_elem<BF16>(ptr, q) : 0.0f;
-                        }
-                        const uint32_t e_first = es[u] > 0 ? static_cast<uint32_t>(es[u]) : 0u;
-                        const uint32_t ca = fdiv(e_first, a.div_hw);
-                        const int32_t kb = static_cast<int32_t>((ca + 1) * HW) - es[u];
-                        const float Ka = Ks[ca], Kb = Ks[ca + 1];
-                        float s_all = 0.0f, q_all = 0.0f, s_hi = 0.0f, q_hi = 0.0f;
-#pragma unroll
-                        for (int q = 0; q < W; ++q) {
-                            const int32_t e = es[u] + q;
-                            const bool valid = e >= 0 && e < run_elems;
-                            const bool hi = q >= kb;
-                            const float d = valid ? __fsub_rn(xe[q], hi ? Kb : Ka) : 0.0f;
-                            const float dh = hi ? d : 0.0f;
-                            s_all += d;
-                            q_all = fmaf(d, d, q_all);
-                            s_hi += dh;
-                            q_hi = fmaf(dh, dh, q_hi);
-                        }
-                        seg[slot[u]] = make_float4(__fsub_rn(s_all, s_hi), __fsub_rn(q_all, q_hi), s_hi, q_hi);
-                    }
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (!interior[u]) continue;                               // interior vector: no masks
-                const uint32_t ca = fdiv(static_cast<uint32_t>(es[u]), a.div_hw);
-                const int32_t kb = static_cast<int32_t>((ca + 1) * HW) - es[u];
-                const float Ka = Ks[ca], Kb = Ks[ca + 1];
-                float s_all = 0.0f, q_all = 0.0f, s_hi = 0.0f, q_hi = 0.0f;
-#pragma unroll
-                for (int q = 0; q < W; ++q) {
-                    const bool hi = q >= kb;
-                    const float d = __fsub_rn(vec_elem<BF16>(raw[u], q), hi ? Kb : Ka);
-                    const float dh = hi ? d : 0.0f;
-                    s_all += d;
-                    q_all = fmaf(d, d, q_all);
-                    s_hi += dh;
-                    q_hi = fmaf(dh, dh, q_hi);
-                }
-                seg[slot[u]] = make_float4(__fsub_rn(s_all, s_hi), __fsub_rn(q_all, q_hi), s_hi, q_hi);
-            }
-        }
-        __syncthreads();
-        // phase B
-        if (jb < nr && cl < Gc) {
-            const uint32_t pre = static_cast<uint32_t>(rpre[jb]);
-            const uint32_t lo = pre + static_cast<uint32_t>(cl) * HW;       // element position in the vector grid
-            const uint32_t hi = lo + HW - 1;
-            for (uint32_t v = lo / W + k; v <= hi / W; v += Tk) {
-                const int32_t e_start = static_cast<int32_t>(v * W) - static_cast<int32_t>(pre);
-                const uint32_t e_first = e_start > 0 ? static_cast<uint32_t>(e_start) : 0u;
-                const float4 sg = seg[jb * vslot + v];
-                if (fdiv(e_first, a.div_hw) == static_cast<uint32_t>(cl)) {
-                    acc_s += sg.x;
-                    acc_q += sg.y;
-                } else {
-                    acc_s += sg.z;
-                    acc_q += sg.w;
-                }
-            }
-        }
-        __syncthreads();
+    for (int m = 0; m < CPL; ++m) {
+        cl[m] = a.G >= 32 ? lane + 32 * m : lane >> a.tc_log2;
+        K[m] = cl[m] < Gc ? load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + cl[m]) * HW) : 0.0f;
+        acc_s[m] = 0.0f;
+        acc_q[m] = 0.0f;
     }
-    red[0][threadIdx.x] = acc_s;
-    red[1][threadIdx.x] = acc_q;
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[1])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    // Copy tile t into buffer t & 1 (warp 0): each lane handles runs lane, lane+32, ...
+    auto issue = [&](int t) {
+        const int tb = p0 + t * R, nr = min(R, p1 - tb);
+        unsigned char* buf = smem + (t & 1) * buf_bytes;
+        uint64_t* b = &bar[t & 1];
+        uint32_t tx = 0;
+        for (int j = lane; j < nr; j += 32) {
+            const uint32_t pl = static_cast<uint32_t>(tb + j);
+            const uint32_t r = fdiv(pl, a.div_batch);
+            const uint32_t bb = pl - r * static_cast<uint32_t>(a.batch);
+            const uint64_t a0 = (static_cast<uint64_t>(bb) * a.C + c0) * HW * ESZ, a1 = a0 + run_bytes;
+            const uint64_t hi = min((a1 + 15) & ~uint64_t(15), a.buf_fl);
+            tx += static_cast<uint32_t>(hi - (a0 & ~uint64_t(15)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tx += __shfl_xor_sync(0xffffffffu, tx, o);
+        if (lane == 0)
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(tx)
+                         : "memory");
+        __syncwarp();
+        for (int j = lane; j < nr; j += 32) {
+            const uint32_t pl = static_cast<uint32_t>(tb + j);
+            const uint32_t r = fdiv(pl, a.div_batch);
+            const uint32_t bb = pl - r * static_cast<uint32_t>(a.batch);
+            const uint64_t a0 = (static_cast<uint64_t>(bb) * a.C + c0) * HW * ESZ, a1 = a0 + run_bytes;
+            const uint64_t a0al = a0 & ~uint64_t(15);
+            const uint64_t hi = min((a1 + 15) & ~uint64_t(15), a.buf_fl);
+            unsigned char* dst = buf + j * a.slot_bytes;
+            const char* src = static_cast<const char*>(a.x[r]);
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                             smem_u32(dst)),
+                         "l"(src + a0al), "r"(static_cast<uint32_t>(hi - a0al)), "r"(smem_u32(b))
+                         : "memory");
+            for (uint64_t q = hi; q < a1; q += ESZ) {             // the buffer ends inside the last block
+                if constexpr (BF16) *reinterpret_cast<unsigned short*>(dst + (q - a0al)) = *reinterpret_cast<const unsigned short*>(src + q);
+                else *reinterpret_cast<float*>(dst + (q - a0al)) = *reinterpret_cast<const float*>(src + q);
+            }
+        }
+    };
+    if (warp == 0) {
+        issue(0);
+        if (ntiles > 1) issue(1);
+    }
+
+    bool failed = false;
+    for (int t = 0; t < ntiles; ++t) {
+        // thread 0 waits for the tile's copies; the others wait at the CTA barrier (no issue slots)
+        bool timed_out = false;
+        const uint32_t parity = static_cast<uint32_t>(t >> 1) & 1u;
+        if (threadIdx.x == 0 && !mbar_try_wait(&bar[t & 1], parity)) {
+            const uint64_t start = global_ns();
+            while (!mbar_try_wait(&bar[t & 1], parity)) {
+                if (global_ns() - start > kCopyWaitNs) {
+                    timed_out = true;
+                    break;
+                }
+            }
+        }
+        if (__syncthreads_or(timed_out)) {                    // also orders warp 0's plain tail stores
+            failed = true;
+            break;
+        }
+        const int tb = p0 + t * R, nr = min(R, p1 - tb);
+        const unsigned char* buf = smem + (t & 1) * buf_bytes;
+        for (int j = warp; j < nr; j += kWarps) {
+            const uint32_t pl = static_cast<uint32_t>(tb + j);
+            const uint32_t r = fdiv(pl, a.div_batch);
+            const uint32_t bb = pl - r * static_cast<uint32_t>(a.batch);
+            const uint32_t pre = static_cast<uint32_t>(((static_cast<uint64_t>(bb) * a.C + c0) * HW * ESZ) & 15u);
+            const unsigned char* run = buf + j * a.slot_bytes;
+#pragma unroll
+            for (int m = 0; m < CPL; ++m) {
+                if (cl[m] < Gc)
+                    sum_range<BF16>(run, pre + (static_cast<uint32_t>(cl[m]) * HW + e_lo) * ESZ, e_hi - e_lo, K[m],
+                                    acc_s[m], acc_q[m]);
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // reads done before the next bulk writes
+        __syncthreads();
+        if (warp == 0 && t + 2 < ntiles) issue(t + 2);
+    }
+
+    // combine: smem holds [warp][m][lane] sums, then one thread per channel adds the warps' and
+    // lanes' shares in a fixed order in float-float
+    float* red_s = reinterpret_cast<float*>(smem);
+    float* red_q = red_s + kWarps * CPL * 32;
+#pragma unroll
+    for (int m = 0; m < CPL; ++m) {
+        red_s[(warp * CPL + m) * 32 + lane] = acc_s[m];
+        red_q[(warp * CPL + m) * 32 + lane] = acc_q[m];
+    }
     __syncthreads();
     if (threadIdx.x < Gc) {
+        const int c = threadIdx.x;
+        const int m = a.G >= 32 ? c / 32 : 0;
+        const int l0 = a.G >= 32 ? c % 32 : c * Tc;
+        const int nl = a.G >= 32 ? 1 : Tc;
         FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
-        for (int jj = 0; jj < a.R; ++jj)
-            for (int q = 0; q < Tk; ++q) {
-                const int t = (jj * a.G + threadIdx.x) * Tk + q;
-                S = ff_add(S, FF{red[0][t], 0.0f});
-                Q = ff_add(Q, FF{red[1][t], 0.0f});
+        for (int w = 0; w < kWarps; ++w)
+            for (int l = l0; l < l0 + nl; ++l) {
+                S = ff_add(S, FF{red_s[(w * CPL + m) * 32 + l], 0.0f});
+                Q = ff_add(Q, FF{red_q[(w * CPL + m) * 32 + l], 0.0f});
             }
-        a.partial[static_cast<int64_t>(c0 + threadIdx.x) * a.S + s] =
-            make_float2(__fadd_rn(S.hi, S.lo), __fadd_rn(Q.hi, Q.lo));
+        a.partial[static_cast<int64_t>(c0 + c) * a.S + s] =
+            failed ? make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000))
+                   : make_float2(__fadd_rn(S.hi, S.lo), __fadd_rn(Q.hi, Q.lo));
     }
 }
 
@@ -343,9 +460,8 @@ __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_c
     constexpr int kWarps = kThreads / 32;
     const int c = blockIdx.x, s = blockIdx.y;
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
-    const int P = a.n * a.batch;
-    const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
-    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
+    int p0, p1;
+    slice_bounds(a, s, p0, p1);
     const uint32_t units = static_cast<uint32_t>(a.HW / W);                     // vectors per plane
     const uint32_t cpp = (units + kChunkVecs - 1) / kChunkVecs;                  // chunks per plane
     const uint32_t total = static_cast<uint32_t>(p1 - p0) * cpp;
@@ -405,9 +521,8 @@ __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_c
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) bn_stats_element_kernel(const __grid_constant__ BnParams a) {
     const int c = blockIdx.x, s = blockIdx.y;
-    const int P = a.n * a.batch;
-    const int p0 = static_cast<int>(static_cast<int64_t>(P) * s / a.S);
-    const int p1 = static_cast<int>(static_cast<int64_t>(P) * (s + 1) / a.S);
+    int p0, p1;
+    slice_bounds(a, s, p0, p1);
     pdl_enter();
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);
     float acc_s = 0.0f, acc_q = 0.0f;
@@ -574,12 +689,76 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
 
 // ---------------------------------------------------------------- launch planning (host)
 
-enum StatsKind { kPlaneVec, kPlaneScalar, kSegment, kStaged };
+// Launch with `smem` bytes of dynamic shared memory and programmatic stream
+// serialisation; the opt-in above 48 KiB is set once per kernel and device.
+int launch_pdl_smem(void (*kernel)(BnParams), dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> granted;   // (kernel, device) -> bytes allowed
+    if (smem > 48 * 1024) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        std::lock_guard<std::mutex> lock(mu);
+        auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+        auto it = granted.find(key);
+        if (it == granted.end() || it->second < smem) {
+            e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem);
+            if (e != cudaSuccess) return cuda_fail(e);
+            granted[key] = smem;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(static_cast<unsigned>(kThreads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return check_launch();
+}
+
+// Channels per lane of the bulk-staged kernel: G/32 for G >= 32 (G <= 256).
+template <bool BF16>
+int launch_bulk(int G, dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
+    switch (G >= 32 ? G / 32 : 1) {
+        case 1: return launch_pdl_smem(bn_stats_bulk_kernel<BF16, 1>, grid, smem, s, p);
+        case 2: return launch_pdl_smem(bn_stats_bulk_kernel<BF16, 2>, grid, smem, s, p);
+        case 4: return launch_pdl_smem(bn_stats_bulk_kernel<BF16, 4>, grid, smem, s, p);
+        default: return launch_pdl_smem(bn_stats_bulk_kernel<BF16, 8>, grid, smem, s, p);
+    }
+}
+
+enum StatsKind { kPlaneVec, kPlaneScalar, kBulk, kStaged };
 
 struct StatsPlan {
     StatsKind kind;
     int G, S, R, slot_bytes;
+    int smem;           // bulk kernel: dynamic shared bytes (two tile buffers)
 };
+
+// Slices of the bulk kernel: about one resident wave of CTAs, so that each
+// CTA streams several tiles through its two buffers.  kWaveSms is GB300's
+// SM count; on another part only the slice count (not the result's
+// correctness) depends on it.
+constexpr int kWaveSms = 152;
+
+int bulk_slices(int n_groups, int P, int C, int smem) {
+    int per_sm = (227 * 1024) / (smem + 1024);              // shared memory per SM, 1 KiB reserved per CTA
+    if (per_sm > 6) per_sm = 6;                             // registers: 6 CTAs of 256 threads
+    if (per_sm < 1) per_sm = 1;
+    int64_t S = static_cast<int64_t>(kWaveSms) * per_sm / n_groups;
+    if (S > P) S = P;
+    const int64_t cap = kMaxPartials / C;
+    if (S > cap) S = cap;
+    if (S < 1) S = 1;
+    return static_cast<int>(S);
+}
 
 int pow2_floor(int v) {
     int p = 1;
@@ -610,7 +789,7 @@ int slot_bytes_for(int G, int HW, int esz) {
 }
 
 // Aligned planes: plane kernel with 16-byte loads.  Unaligned planes at
-// least one vector long: segment kernel.  Planes shorter than a vector:
+// least one vector long: bulk-staged kernel.  Planes shorter than a vector:
 // staged group kernel.  Unaligned planes too long to fit a group's run in
 // the shared buffer: plane kernel with element loads.
 StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
@@ -622,13 +801,19 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
     const bool fits = slot <= kStageBytes;
     if (HW % W == 0) sp.kind = kPlaneVec;
     else if (!fits) sp.kind = kPlaneScalar;
-    else sp.kind = HW >= W ? kSegment : kStaged;
-    if (sp.kind == kSegment || sp.kind == kStaged) {
+    else sp.kind = HW >= W ? kBulk : kStaged;
+    if (sp.kind == kBulk) {
+        sp.G = G;
+        sp.slot_bytes = slot;
+        sp.R = kBulkBufMax / slot < kBulkRuns ? kBulkBufMax / slot : kBulkRuns;
+        const int cpl = G >= 32 ? G / 32 : 1;
+        const int red = kThreads * cpl * 2 * static_cast<int>(sizeof(float));
+        sp.smem = 2 * sp.R * slot > red ? 2 * sp.R * slot : red;
+        sp.S = bulk_slices((C + G - 1) / G, P, C, sp.smem);
+    } else if (sp.kind == kStaged) {
         sp.G = G;
         sp.slot_bytes = slot;
         sp.R = kStageBytes / slot;
-        if (sp.kind == kSegment && sp.R > kThreads / G) sp.R = kThreads / G;   // one (run, channel) pair per thread
-        if (sp.kind == kSegment && sp.R > kMaxRuns) sp.R = kMaxRuns;
         sp.S = slices_for((C + G - 1) / G, P, C);
     } else {
         sp.G = 1;
@@ -741,23 +926,27 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     p.G = sp.G;
     p.R = sp.R;
     p.slot_bytes = sp.slot_bytes;
+    p.buf_fl = (static_cast<uint64_t>(batch) * C * p.HW * esz) & ~uint64_t(15);
+    p.tc_log2 = 0;
+    while (sp.G < 32 && (sp.G << p.tc_log2) < 32) ++p.tc_log2;
     p.eps = eps;
     char* ws = static_cast<char*>(workspace);
     p.partial = reinterpret_cast<float2*>(ws);
     ws += align_up(static_cast<size_t>(C) * p.S * sizeof(float2), 16);
     p.coef = reinterpret_cast<float4*>(ws);
     p.div_batch = make_fastdiv(static_cast<uint32_t>(batch));
+    p.ps_small = static_cast<int64_t>(n_replicas) * batch * sp.S < (int64_t(1) << 31) ? 1 : 0;
+    if (p.ps_small) p.div_s = make_fastdiv(static_cast<uint32_t>(sp.S));
     p.div_hw = make_fastdiv(static_cast<uint32_t>(p.HW));
     p.div_c = make_fastdiv(static_cast<uint32_t>(C));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int st;
-    if (sp.kind == kSegment || sp.kind == kStaged) {
+    if (sp.kind == kBulk || sp.kind == kStaged) {
         p.div_unit = make_fastdiv(static_cast<uint32_t>(sp.slot_bytes / 16));
         const dim3 grid(static_cast<unsigned>((C + sp.G - 1) / sp.G), static_cast<unsigned>(sp.S));
-        if (sp.kind == kSegment)
-            st = bf16_in ? launch_pdl(bn_stats_segment_kernel<true>, grid, kThreads, s, p)
-                         : launch_pdl(bn_stats_segment_kernel<false>, grid, kThreads, s, p);
+        if (sp.kind == kBulk)
+            st = bf16_in ? launch_bulk<true>(sp.G, grid, sp.smem, s, p) : launch_bulk<false>(sp.G, grid, sp.smem, s, p);
         else
             st = bf16_in ? launch_pdl(bn_stats_group_kernel<true>, grid, kThreads, s, p)
                          : launch_pdl(bn_stats_group_kernel<false>, grid, kThreads, s, p);
