@@ -33,11 +33,12 @@
 //      reductions) and stores one fp32 (sum, sum of squares) partial per
 //      channel and slice.
 //   2. merge  — one warp per channel sums the S partials in a fixed order in
-//      float-float (fp32 pairs), then one thread per channel finalises in
-//      fp64: with m' = Σd/M, mean = K_c + m', var = Σd²/M − m'² (the same
-//      S/M and Q/M − mean² up to rounding), invstd = 1/sqrt(var + eps); it
-//      stores per channel (m_hi, m_lo, scale, β) where m_hi + m_lo is the
-//      mean as an fp32 pair and scale = invstd·γ.
+//      float-float (fp32 pairs), then one thread per channel finalises: in
+//      fp64, with m' = Σd/M, mean = K_c + m' and var = Σd²/M − m'² (the same
+//      S/M and Q/M − mean² up to rounding); in fp32, invstd =
+//      1/sqrt(var + eps) with IEEE-rounded sqrt and divide.  It stores per
+//      channel (m_hi, m_lo, scale, β) where m_hi + m_lo is the mean as an
+//      fp32 pair and scale = invstd·γ.
 //   3. apply  — y = ((x − m_hi) − m_lo)·scale + β over every replica, 16-byte
 //      vectors in and out, the channel computed once per 8-element vector.
 //      x − m_hi is exact when x is near the mean (Sterbenz), so no
@@ -82,6 +83,7 @@ struct BnParams {
     int32_t tc_log2;    // bulk kernel: log2 of the lanes per channel (32/G for G < 32, else 0)
     uint64_t buf_fl;    // bulk kernel: replica bytes rounded down to 16 (copies stop there)
     float eps;
+    double inv_count;   // 1 / (n * batch * H * W)
 };
 
 template <bool BF16>
@@ -553,7 +555,15 @@ __global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_co
     __shared__ FF sums[2][32];
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int c = blockIdx.x * 32 + w;
+    const int cc = blockIdx.x * 32 + lane;   // warp 0: the channel this lane finalises
     pdl_enter();
+    // warp 0 fetches its channels' shift K, gamma and beta while the partials are summed
+    float Kc = 0.0f, gc = 1.0f, bc = 0.0f;
+    if (w == 0 && cc < a.C) {
+        Kc = load_elem<BF16>(a.x[0], static_cast<int64_t>(cc) * a.HW);
+        if (a.gamma) gc = a.gamma[cc];
+        if (a.beta) bc = a.beta[cc];
+    }
     FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
     if (c < a.C) {
         const float2* p = a.partial + static_cast<int64_t>(c) * a.S;
@@ -579,24 +589,19 @@ __global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_co
         sums[1][w] = Q;
     }
     __syncthreads();
-    if (w != 0) return;
-    const int cc = blockIdx.x * 32 + lane;
-    if (cc >= a.C) return;
+    if (w != 0 || cc >= a.C) return;
+    // fp64: the sums, the mean and the variance; fp32: 1/sqrt(var + eps) (IEEE sqrt and divide,
+    // relative error ~2^-23, far inside what the normalisation needs) and the scale
     const double Sd = static_cast<double>(sums[0][lane].hi) + static_cast<double>(sums[0][lane].lo);
     const double Qd = static_cast<double>(sums[1][lane].hi) + static_cast<double>(sums[1][lane].lo);
-    const double M = static_cast<double>(a.n) * a.batch * a.HW;
-    const double K = static_cast<double>(load_elem<BF16>(a.x[0], static_cast<int64_t>(cc) * a.HW));
-    const double ms = Sd / M;
-    const double mean = K + ms;
-    const double var = Qd / M - ms * ms;
-    const double invstd = 1.0 / sqrt(var + static_cast<double>(a.eps));
-    const double g = a.gamma ? static_cast<double>(a.gamma[cc]) : 1.0;
-    const double b = a.beta ? static_cast<double>(a.beta[cc]) : 0.0;
+    const double ms = Sd * a.inv_count;                    // mean of the shifted values
+    const double mean = static_cast<double>(Kc) + ms;
+    const double var = Qd * a.inv_count - ms * ms;
+    const float invstd = 1.0f / sqrtf(static_cast<float>(var + static_cast<double>(a.eps)));
     const float m_hi = static_cast<float>(mean);
     a.mean_out[cc] = m_hi;
-    a.invstd_out[cc] = static_cast<float>(invstd);
-    a.coef[cc] = make_float4(m_hi, static_cast<float>(mean - static_cast<double>(m_hi)),
-                             static_cast<float>(invstd * g), static_cast<float>(b));
+    a.invstd_out[cc] = invstd;
+    a.coef[cc] = make_float4(m_hi, static_cast<float>(mean - static_cast<double>(m_hi)), invstd * gc, bc);
 }
 
 // ((x − m_hi) − m_lo)·scale + β with k = (m_hi, m_lo, scale, β)
@@ -930,6 +935,7 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     p.tc_log2 = 0;
     while (sp.G < 32 && (sp.G << p.tc_log2) < 32) ++p.tc_log2;
     p.eps = eps;
+    p.inv_count = 1.0 / (static_cast<double>(n_replicas) * batch * p.HW);
     char* ws = static_cast<char*>(workspace);
     p.partial = reinterpret_cast<float2*>(ws);
     ws += align_up(static_cast<size_t>(C) * p.S * sizeof(float2), 16);
