@@ -59,7 +59,9 @@ namespace {
 constexpr int kTargetCtas = 2048;        // stats CTAs aimed for (about two waves on 152 SMs)
 constexpr int64_t kMaxPartials = 65536;  // C*S bound: fp32 partials stay <= 512 KiB
 constexpr int kRunElems = 2048;          // channels per group: G*H*W <= this (G >= 1)
-constexpr int kStageBytes = 32768;       // shared staging / segment buffer per CTA
+constexpr int kStageBytes = 32768;       // shared staging buffer per CTA (staged group kernel)
+constexpr int kApplyWaves = 8;           // apply grid: at most this many waves of resident CTAs
+constexpr int kApplyVecs = 8;            // apply grid: at least this many 16-byte vectors per thread
 
 struct BnParams {
     const void* x[DDP_MAX_REPLICAS];
@@ -978,9 +980,11 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     DeviceInfo d;
     if ((st = current_device_info(&d)) != DDP_OK) return st;
     const int64_t nvec = static_cast<int64_t>(E / 8);
-    int64_t gx = (nvec + kThreads - 1) / kThreads;
+    // at least kApplyVecs vectors per thread (two passes of its 4-vector unroll), and at most
+    // kApplyWaves waves of resident CTAs: several waves stream faster than one grid-stride wave
+    int64_t gx = (nvec + static_cast<int64_t>(kThreads) * kApplyVecs - 1) / (static_cast<int64_t>(kThreads) * kApplyVecs);
     const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
-    int64_t cap = (resident + n_replicas - 1) / n_replicas;
+    int64_t cap = (kApplyWaves * resident + n_replicas - 1) / n_replicas;
     if (gx > cap) gx = cap;
     if (gx < 1) gx = 1;
     const dim3 agrid(static_cast<unsigned>(gx), static_cast<unsigned>(n_replicas));
