@@ -298,12 +298,32 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
 
 // One wave of CTAs (at most max_grid) for a bucket of nvec 16-byte vectors,
 // then a PDL launch.
+// Grid of the streaming kernels.  One grid-stride wave of resident CTAs is
+// the default; a launch long enough that one wave would give every thread
+// at least kMultiWaveVecs vectors gets up to kWaves waves instead (each
+// thread still at least kMinVecsPerThread vectors).  Measured on GB300:
+// fused SGD over GPT-2-small buckets 6.58 -> 7.24 TB/s and the bf16 average
+// 6.89 -> 7.19 TB/s with 16 waves, while 25 MiB fp32 buckets (14 vectors per
+// thread at one wave) ran 3 % slower with several.
+constexpr int kWaves = 16;
+constexpr int64_t kMultiWaveVecs = 32;
+constexpr int64_t kMinVecsPerThread = 8;
+
 template <typename Params>
 int launch_wave(void (*kernel)(Params), int64_t nvec, cudaStream_t s, const Params& p, int max_grid = 1 << 30) {
-    int grid = 0;
-    const int st = one_wave_grid(reinterpret_cast<const void*>(kernel), kThreads,
-                                 (nvec + kThreads - 1) / kThreads, &grid);
+    int wave = 0;
+    const int st = one_wave_grid(reinterpret_cast<const void*>(kernel), kThreads, INT64_MAX, &wave);
     if (st != DDP_OK) return st;
+    const int64_t threads = static_cast<int64_t>(wave) * kThreads;
+    int64_t g = (nvec + kThreads - 1) / kThreads;                 // one vector per thread at most
+    if (nvec >= kMultiWaveVecs * threads) {
+        g = (nvec + kThreads * kMinVecsPerThread - 1) / (kThreads * kMinVecsPerThread);
+        if (g > static_cast<int64_t>(kWaves) * wave) g = static_cast<int64_t>(kWaves) * wave;
+    } else if (g > wave) {
+        g = wave;
+    }
+    if (g < 1) g = 1;
+    int grid = static_cast<int>(g);
     if (grid > max_grid) grid = max_grid;
     return launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), kThreads, s, p);
 }
