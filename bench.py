@@ -636,30 +636,37 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                                 "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
                                 "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
                                 "launches": 1, "calls_per_graph": SAMPLER_CALLS}
-    # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point)
+    # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point): 1 KiB .. 1 GiB
+    # per replica in x4 steps, N in {2, 4, 8, 16}, caps {1, 25, 100} MiB; a cap that does not change the
+    # launch count is measured once; the 1 MiB split also as grouped launches (up to 1024 buckets each)
     sweep = []
-    for size in (4 << 20, 64 << 20, 1 << 30):
+    for size in [1 << (10 + 2 * k) for k in range(11)]:
         numel = size // 4
-        for n in (2, 8, 16):
+        for n in (2, 4, 8, 16):
             reps = [workloads.device_normal((numel,), 0.0, 1.0, workloads.seed_for(5, r), device=dev)
                     for r in range(n)]
             outs = torch.empty(numel, device=dev)
+            nbytes = (n + 1) * size
+            l2 = "working set in L2" if nbytes < L2_BYTES else "larger than L2"
+            iters = 200 if size <= (64 << 20) else 20
+            seen = set()
             for cap in (1 << 20, 25 << 20, 100 << 20):
                 ce = cap // 4
+                nl = -(-numel // ce)
+                if nl in seen:
+                    continue
+                seen.add(nl)
 
                 def flat_step(reps=reps, outs=outs, ce=ce, numel=numel):
                     for s0 in range(0, numel, ce):
                         e = min(numel, s0 + ce)
                         g.ddp_bucket_allreduce_mean([x[s0:e] for x in reps], outs[s0:e])
-                iters = 200 if size <= (64 << 20) else 20
                 ms = _time_launches(torch, flat_step, iters, side)
-                nbytes = (n + 1) * size
-                sweep.append({"bytes_per_replica": size, "replicas": n, "cap_mib": cap >> 20,
-                              "launches": -(-numel // ce), "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
-                              "frac": nbytes / ms / 1e6 / peak,
-                              "l2": "working set in L2" if (n + 1) * size < L2_BYTES else "larger than L2"})
-                if cap == (1 << 20):
-                    # the same buckets averaged by one grouped launch (up to 1024 buckets per launch)
+                sweep.append({"bytes_per_replica": size, "replicas": n,
+                              "cap_mib": cap >> 20 if nl > 1 else "any (one launch)",
+                              "launches": nl, "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
+                              "frac": nbytes / ms / 1e6 / peak, "l2": l2})
+                if nl > 1 and cap == (1 << 20):
                     bl = [(s0, min(ce, numel - s0)) for s0 in range(0, numel, ce)]
 
                     def grouped(reps=reps, outs=outs, bl=bl):
@@ -668,8 +675,7 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                     ms = _time_launches(torch, grouped, iters, side)
                     sweep.append({"bytes_per_replica": size, "replicas": n, "cap_mib": 1,
                                   "launches": -(-len(bl) // 1024), "grouped": True, "us": ms * 1e3,
-                                  "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-                                  "l2": "working set in L2" if (n + 1) * size < L2_BYTES else "larger than L2"})
+                                  "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "l2": l2})
             del reps, outs
     rows["sweep_flat_fp32"] = sweep
     rows["_peak"] = {"hbm_gbs": peak, "source": peak_kind}
