@@ -34,7 +34,7 @@ struct AccParams {
     int64_t numel;
 };
 
-// grid (x: one wave over vectors, y: replica)
+// grid (x: CTAs over the vectors, grid-stride, y: replica)
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) accumulate_kernel(const __grid_constant__ AccParams a) {
     constexpr int VEC = BF16 ? 8 : 4;

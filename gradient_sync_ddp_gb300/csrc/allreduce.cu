@@ -12,10 +12,11 @@
 // each thread streams one 16-byte vector from every replica (all N loads are
 // issued before the first add, N*16 bytes in flight per thread), keeps the
 // adds in the exact rank order with __fadd_rn (no contraction), and writes
-// the fp32 result with a streaming store.  The grid is exactly one wave
-// (resident CTAs per SM from the occupancy calculator x SMs) and strides over
-// the bucket, so no partial last wave idles SMs; launches use programmatic
-// dependent launch so back-to-back bucket kernels overlap launch and tail.  The
+// the fp32 result with a streaming store.  The grid strides over the bucket:
+// one wave of resident CTAs (occupancy calculator x SMs) for ordinary
+// buckets, several waves for launches long enough to give each thread many
+// vectors (see launch_wave); launches use programmatic dependent launch so
+// back-to-back bucket kernels overlap launch and tail.  The
 // replica pointers travel in a __grid_constant__ parameter block, so a
 // launch is self-contained and capturable into a CUDA Graph.
 #include <cstdint>
@@ -296,8 +297,6 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
 
 // ---------------------------------------------------------------- host side
 
-// One wave of CTAs (at most max_grid) for a bucket of nvec 16-byte vectors,
-// then a PDL launch.
 // Grid of the streaming kernels.  One grid-stride wave of resident CTAs is
 // the default; a launch long enough that one wave would give every thread
 // at least kMultiWaveVecs vectors gets up to kWaves waves instead (each
