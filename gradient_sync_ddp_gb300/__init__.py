@@ -394,3 +394,77 @@ def ddp_bucket_allreduce_mean_multi(replica_bases, buckets, out_base, stream=Non
 
 
 __all__ += ["ddp_bucket_allreduce_mean_multi", "MULTI_MAX_BUCKETS"]
+
+
+# ---------------------------------------------------------------- bucket readiness (host only)
+
+_lib.ddp_reducer_create.argtypes = [_c.c_int32, _P, _c.c_int32, _P]
+_lib.ddp_reducer_create.restype = _c.c_int
+_lib.ddp_reducer_destroy.argtypes = [_P]
+_lib.ddp_reducer_destroy.restype = None
+for _name in ("ddp_reducer_mark_ready", "ddp_reducer_mark_unused"):
+    getattr(_lib, _name).argtypes = [_P, _c.c_int32, _P]
+    getattr(_lib, _name).restype = _c.c_int
+_lib.ddp_reducer_wait_all.argtypes = [_P, _c.c_int64, _P]
+_lib.ddp_reducer_wait_all.restype = _c.c_int
+_lib.ddp_reducer_reset.argtypes = [_P]
+_lib.ddp_reducer_reset.restype = _c.c_int
+_lib.ddp_reducer_completed.argtypes = [_P, _P, _c.c_int32, _P]
+_lib.ddp_reducer_completed.restype = _c.c_int
+
+
+def ddp_reducer_create(tensor_bucket, n_buckets: int) -> int:
+    """Tracker handle for parameters whose buckets are tensor_bucket[t]."""
+    T = len(tensor_bucket)
+    arr = (ctypes.c_int32 * max(1, T))(*[int(b) for b in tensor_bucket])
+    h = ctypes.c_void_p(0)
+    _check(_lib.ddp_reducer_create(T, ctypes.addressof(arr), int(n_buckets), ctypes.addressof(h)),
+           "ddp_reducer_create")
+    return h.value
+
+
+def ddp_reducer_destroy(handle) -> None:
+    _lib.ddp_reducer_destroy(handle)
+
+
+def ddp_reducer_mark_ready(handle, tensor: int) -> int:
+    """Mark a parameter's gradient ready; returns the bucket this completed, or -1."""
+    b = ctypes.c_int32(-1)
+    _check(_lib.ddp_reducer_mark_ready(handle, int(tensor), ctypes.addressof(b)), "ddp_reducer_mark_ready")
+    return b.value
+
+
+def ddp_reducer_mark_unused(handle, tensor: int) -> int:
+    """Mark a parameter unused in this iteration; returns the bucket this completed, or -1."""
+    b = ctypes.c_int32(-1)
+    _check(_lib.ddp_reducer_mark_unused(handle, int(tensor), ctypes.addressof(b)), "ddp_reducer_mark_unused")
+    return b.value
+
+
+def ddp_reducer_wait_all(handle, timeout_us: int):
+    """(True, -1) when every bucket is complete; (False, first unmarked
+    parameter) when the wait ran out (DDP_ERR_TIMEOUT).  Other errors raise."""
+    m = ctypes.c_int32(-1)
+    st = _lib.ddp_reducer_wait_all(handle, int(timeout_us), ctypes.addressof(m))
+    if st == DDP_ERR_TIMEOUT:
+        return False, m.value
+    _check(st, "ddp_reducer_wait_all")
+    return True, m.value
+
+
+def ddp_reducer_reset(handle) -> None:
+    _check(_lib.ddp_reducer_reset(handle), "ddp_reducer_reset")
+
+
+def ddp_reducer_completed(handle) -> list:
+    """Buckets completed so far in this iteration, in completion order."""
+    n = ctypes.c_int32(0)
+    _check(_lib.ddp_reducer_completed(handle, None, 0, ctypes.addressof(n)), "ddp_reducer_completed")
+    arr = (ctypes.c_int32 * max(1, n.value))()
+    _check(_lib.ddp_reducer_completed(handle, ctypes.addressof(arr), n.value, ctypes.addressof(n)),
+           "ddp_reducer_completed")
+    return list(arr[:n.value])
+
+
+__all__ += ["ddp_reducer_create", "ddp_reducer_destroy", "ddp_reducer_mark_ready", "ddp_reducer_mark_unused",
+            "ddp_reducer_wait_all", "ddp_reducer_reset", "ddp_reducer_completed"]

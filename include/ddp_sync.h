@@ -118,6 +118,70 @@ int ddp_plan_buckets(int32_t n_tensors, const int64_t* numels, int32_t elem_byte
                      int64_t* total_elems);
 
 /*
+ * Bucket readiness (the reducer's bookkeeping; host side, no CUDA call).
+ *
+ * [DDP] §3.2 and §4.2: every parameter's gradient hook marks the parameter
+ * ready in its bucket, and a bucket's all-reduce is issued as soon as all of
+ * its parameters are ready, while backward still runs for earlier layers.
+ * [DDP] §3.3: a parameter skipped by the forward pass never gets a gradient,
+ * so its bucket never completes and the job waits forever;
+ * find_unused_parameters marks such parameters as needing no communication.
+ * Here marking a parameter unused counts it as ready: its gradient slice is
+ * averaged as it stands, so the caller zeroes it for the step, as PyTorch's
+ * reducer does.  The wait for the remaining buckets is bounded and reports
+ * the first parameter that was never marked instead of hanging.
+ *
+ * All functions are thread-safe (hooks may fire on several threads).  The
+ * tracker copies what it needs from the arguments; the caller frees nothing
+ * but the tracker itself (ddp_reducer_destroy).
+ */
+typedef struct ddp_reducer ddp_reducer;   /* opaque */
+
+/*
+ * ddp_reducer_create — tracker for n_tensors parameters in n_buckets buckets.
+ *   tensor_bucket  host int32[n_tensors]: bucket of each parameter (as from
+ *                  ddp_plan_buckets), each in [0, n_buckets); every bucket
+ *                  must hold at least one parameter
+ *   out            receives the tracker
+ * DDP_ERR_INVALID_ARG on a bad count, bucket index or empty bucket.
+ */
+int ddp_reducer_create(int32_t n_tensors, const int32_t* tensor_bucket, int32_t n_buckets, ddp_reducer** out);
+
+/* Free the tracker (NULL is allowed). */
+void ddp_reducer_destroy(ddp_reducer* r);
+
+/*
+ * ddp_reducer_mark_ready — parameter `tensor`'s gradient is ready.
+ *   bucket_done  receives the bucket this mark completed (all of its
+ *                parameters now marked; the caller launches its average),
+ *                or -1.  Each bucket is reported exactly once per iteration.
+ * DDP_ERR_INVALID_ARG if tensor is out of range or already marked in this
+ * iteration (a gradient hook fired twice).
+ */
+int ddp_reducer_mark_ready(ddp_reducer* r, int32_t tensor, int32_t* bucket_done);
+
+/* ddp_reducer_mark_unused — like mark_ready, for a parameter the forward
+ * pass did not use in this iteration ([DDP] §3.3, find_unused_parameters). */
+int ddp_reducer_mark_unused(ddp_reducer* r, int32_t tensor, int32_t* bucket_done);
+
+/*
+ * ddp_reducer_wait_all — wait until every bucket of this iteration is
+ * complete, for at most timeout_us microseconds (>= 0; 0 only checks).
+ *   first_missing  receives the lowest parameter index not yet marked, or -1
+ *                  when all are (may be NULL)
+ * DDP_OK when all buckets are complete; DDP_ERR_TIMEOUT when the time ran
+ * out first (the [DDP] §3.3 hang, reported instead of waited out).
+ */
+int ddp_reducer_wait_all(ddp_reducer* r, int64_t timeout_us, int32_t* first_missing);
+
+/* Start the next iteration: every parameter unmarked, no bucket complete. */
+int ddp_reducer_reset(ddp_reducer* r);
+
+/* Buckets completed so far in this iteration, in completion order: writes up
+ * to max_out bucket indices into order_out and the count into *n_done. */
+int ddp_reducer_completed(const ddp_reducer* r, int32_t* order_out, int32_t max_out, int32_t* n_done);
+
+/*
  * ddp_bucket_allreduce_mean — average one bucket over N replicas.
  *
  * [TR24] §一: grad_sync = 0; for r in 0..N-1: grad_sync += grad[r];
