@@ -47,6 +47,7 @@ L2_BYTES = 129 * 10 ** 6
 # Warp instructions one sampler launch issues on the ImageNet-size workload (1,281,168 output
 # slots), by pipe, from an ncu capture of this launch.  The integer ALU and the FMA-heavy
 # pipe each take 2 warp instructions per SM cycle; the four schedulers issue 4 per SM cycle.
+STEP_STREAMS = 8       # streams the headline step's bucket launches are spread over
 SYNCBN_CALLS = 10      # calls captured per graph in the SyncBN rows
 SAMPLER_CALLS = 20     # calls (epochs 1..20) captured per graph in the sampler row
 SAMPLER_WARP_INST = {"alu": 2_706_042, "fmaheavy": 2_147_028, "all": 6_238_443}
@@ -319,20 +320,31 @@ def run_ours(args, world, rank, local):
     out = torch.empty(total, device=dev)
     side = torch.cuda.Stream(device=dev)
 
-    def launch(b):
+    def launch(b, stream=None):
         off, n = buckets[b][0], buckets[b][1]
-        g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps], out[off:off + n])
+        g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps], out[off:off + n], stream=stream)
 
-    # capture one step (the 5 bucket launches, in bucket order) as one graph on the side stream
+    # One step = the bucket launches in bucket order.  The buckets are disjoint, so each goes out on its own
+    # stream (a pool of up to STEP_STREAMS, forked from and joined back into the side stream): a bucket's
+    # CTAs then start on the SMs the previous bucket's last CTAs free, instead of after its whole grid.
+    bucket_streams = [torch.cuda.Stream() for _ in range(min(len(buckets), STEP_STREAMS))]
+
+    def step_body():
+        cur = torch.cuda.current_stream()
+        for st in bucket_streams:
+            st.wait_stream(cur)
+        for b in range(len(buckets)):
+            launch(b, bucket_streams[b % len(bucket_streams)])
+        for st in bucket_streams:
+            cur.wait_stream(st)
+
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        for b in range(len(buckets)):
-            launch(b)
+        step_body()
     torch.cuda.synchronize()
     step_graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(step_graph, stream=side):
-        for b in range(len(buckets)):
-            launch(b)
+        step_body()
     torch.cuda.synchronize()
 
     step_bytes = algorithmic_bytes(plan)
@@ -479,6 +491,9 @@ def run_ours(args, world, rank, local):
                                   "note": "e2e is bound by the host link: the zero-copy kernels read host "
                                           "memory at the rate copy-engine H2D copies reach"}},
             "gpu_launches": K * nb,
+            "schedule": {"graph": "one CUDA graph per step", "bucket_streams": len(bucket_streams),
+                         "note": "each bucket launch on its own stream: the buckets are disjoint, so a bucket's "
+                                 "CTAs start on the SMs the previous bucket frees"},
             "clocks": clocks,
         }
         if rows is not None:
