@@ -529,12 +529,26 @@ def _time_launches(torch, fn, iters, stream):
     return a.elapsed_time(b) / iters
 
 
+def _fan_out(torch, calls, streams):
+    """Run calls[i] on streams[i % len(streams)], forked from and joined back
+    into the current stream (independent buckets overlap; capturable)."""
+    cur = torch.cuda.current_stream()
+    for st in streams:
+        st.wait_stream(cur)
+    for i, call in enumerate(calls):
+        with torch.cuda.stream(streams[i % len(streams)]):
+            call()
+    for st in streams:
+        cur.wait_stream(st)
+
+
 def bench_rows(g, torch, dev, peak, peak_kind):
     """The other rows of the hot path, each on its own workload (not part of
     the headline value): fused SGD on GPT-2 small, SyncBN on the four
     activation shapes, the ImageNet-size sampler, and the bf16 average."""
     import workloads
     side = torch.cuda.Stream(device=dev)
+    pool = [torch.cuda.Stream(device=dev) for _ in range(2)]   # the two GPT-2 buckets are disjoint
     rows = {}
 
     # fused SGD, GPT-2 small DEEP/FIRST, bf16 grads, momentum 0.9, wd 1e-4
@@ -548,9 +562,9 @@ def bench_rows(g, torch, dev, peak, peak_kind):
     buf = torch.zeros(total, device=dev)
 
     def sgd_step():
-        for off, n, _, _ in plan["buckets"]:
-            g.ddp_bucket_allreduce_sgd([x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n],
-                                       0.1, 0.9, 1e-4)
+        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_sgd(
+            [x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4)
+            for off, n, _, _ in plan["buckets"]], pool)
     ms = _time_launches(torch, sgd_step, 50, side)
     nbytes = sum((2 * N_REPLICAS + 16) * b[1] for b in plan["buckets"])
     rows["sgd_gpt2_small"] = {"workload": "GPT-2 small (124,439,808 params), 8 bf16 replicas, DEEP/FIRST buckets, "
@@ -561,9 +575,9 @@ def bench_rows(g, torch, dev, peak, peak_kind):
     low = torch.empty(total, dtype=torch.bfloat16, device=dev)
 
     def sgd_cast_step():
-        for off, n, _, _ in plan["buckets"]:
-            g.ddp_bucket_allreduce_sgd_cast([x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n],
-                                            0.1, 0.9, 1e-4, low[off:off + n])
+        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_sgd_cast(
+            [x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, low[off:off + n])
+            for off, n, _, _ in plan["buckets"]], pool)
     ms = _time_launches(torch, sgd_cast_step, 50, side)
     nbytes = sum((2 * N_REPLICAS + 18) * b[1] for b in plan["buckets"])
     rows["sgd_cast_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, SGD momentum 0.9 wd 1e-4 plus the "
@@ -575,8 +589,9 @@ def bench_rows(g, torch, dev, peak, peak_kind):
     outb = torch.empty(total, device=dev)
 
     def mean_bf16():
-        for off, n, _, _ in plan["buckets"]:
-            g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps], outb[off:off + n])
+        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps],
+                                                                          outb[off:off + n])
+                         for off, n, _, _ in plan["buckets"]], pool)
     ms = _time_launches(torch, mean_bf16, 50, side)
     nbytes = sum((2 * N_REPLICAS + 4) * b[1] for b in plan["buckets"])
     rows["mean_bf16_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, DEEP/FIRST, average to fp32",
@@ -603,11 +618,13 @@ def bench_rows(g, torch, dev, peak, peak_kind):
     coef = torch.empty(1, device=dev)
 
     def clipped_step():
-        for b, (off, n, _, _) in enumerate(plan4["buckets"]):
-            g.ddp_bucket_allreduce_mean_norm([x[off:off + n] for x in acc], gavg[off:off + n], ws, b)
+        _fan_out(torch, [lambda b=b, off=off, n=n: g.ddp_bucket_allreduce_mean_norm(
+            [x[off:off + n] for x in acc], gavg[off:off + n], ws, b)
+            for b, (off, n, _, _) in enumerate(plan4["buckets"])], pool)
         g.ddp_grad_norm_finalize(ws, len(plan4["buckets"]), 1.0, None, coef, None)
-        for off, n, _, _ in plan4["buckets"]:
-            g.ddp_bucket_sgd(gavg[off:off + n], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, grad_scale=coef)
+        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_sgd(
+            gavg[off:off + n], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, grad_scale=coef)
+            for off, n, _, _ in plan4["buckets"]], pool)
     ms = _time_launches(torch, clipped_step, 20, side)
     nbytes = sum(((N_REPLICAS + 1) * 4 + 20) * b[1] for b in plan4["buckets"])
     rows["clipped_step_gpt2_small"] = {"workload": "GPT-2 small, 8 fp32 accumulated replicas: average with norm "
