@@ -471,7 +471,11 @@ __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_c
     const uint32_t total = static_cast<uint32_t>(p1 - p0) * cpp;
     pdl_enter();
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
-    float acc_s = 0.0f, acc_q = 0.0f;
+    // one (Σd, Σd²) pair per element position of the vector: each sums one element per vector (as
+    // many terms as a per-vector total would), at one add and one fused multiply-add per element
+    float ps[W], pq[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) ps[k] = pq[k] = 0.0f;
     for (uint32_t ch0 = warp; ch0 < total; ch0 += 2 * kWarps) {
         uint4 raw[2][2];
         bool ok[2][2];
@@ -497,24 +501,22 @@ __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_c
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 if (!ok[i][u]) continue;
-                float e[W], q[W];
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
-                    e[k] = __fsub_rn(vec_elem<BF16>(raw[i][u], k), K);
-                    q[k] = e[k] * e[k];
+                    const float d = __fsub_rn(vec_elem<BF16>(raw[i][u], k), K);
+                    ps[k] += d;
+                    pq[k] = fmaf(d, d, pq[k]);
                 }
-#pragma unroll
-                for (int w = W; w > 1; w >>= 1)
-#pragma unroll
-                    for (int k = 0; k < w / 2; ++k) {
-                        e[k] = e[2 * k] + e[2 * k + 1];
-                        q[k] = q[2 * k] + q[2 * k + 1];
-                    }
-                acc_s += e[0];
-                acc_q += q[0];
             }
     }
-    FF fs{acc_s, 0.0f}, fq{acc_q, 0.0f};
+#pragma unroll
+    for (int w = W; w > 1; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w / 2; ++k) {
+            ps[k] = ps[2 * k] + ps[2 * k + 1];
+            pq[k] = pq[2 * k] + pq[2 * k + 1];
+        }
+    FF fs{ps[0], 0.0f}, fq{pq[0], 0.0f};
     block_sum2_ff(fs, fq);
     if (threadIdx.x == 0)
         a.partial[static_cast<int64_t>(c) * a.S + s] = make_float2(__fadd_rn(fs.hi, fs.lo), __fadd_rn(fq.hi, fq.lo));
