@@ -468,3 +468,26 @@ def ddp_reducer_completed(handle) -> list:
 
 __all__ += ["ddp_reducer_create", "ddp_reducer_destroy", "ddp_reducer_mark_ready", "ddp_reducer_mark_unused",
             "ddp_reducer_wait_all", "ddp_reducer_reset", "ddp_reducer_completed"]
+
+
+# ---------------------------------------------------------------- sampler resume
+
+_lib.dist_sampler_indices_from.argtypes = [_c.c_int64, _c.c_int32, _c.c_int32, _c.c_uint64, _c.c_uint64,
+                                           _c.c_int32, _c.c_int32, _c.c_int64, _P, _c.c_int64, _P, _P, _P]
+_lib.dist_sampler_indices_from.restype = _c.c_int
+
+
+def dist_sampler_indices_from(n_items: int, n_replicas: int, rank: int, seed: int, epoch: int, shuffle: bool,
+                              drop_last: bool, start: int, out, walk_status=None, stream=None) -> int:
+    """dist_sampler_indices from list position `start` on (resuming an
+    epoch); out holds num_samples - start indices per rank.  Returns num_samples."""
+    ns = ctypes.c_int64(0)
+    _check(_lib.dist_sampler_indices_from(n_items, n_replicas, rank, seed & (2 ** 64 - 1), epoch & (2 ** 64 - 1),
+                                          int(bool(shuffle)), int(bool(drop_last)), int(start), _ptr(out),
+                                          0 if out is None else out.numel(), ctypes.addressof(ns),
+                                          _ptr(walk_status), _stream_ptr(stream)),
+           "dist_sampler_indices_from")
+    return ns.value
+
+
+__all__ += ["dist_sampler_indices_from"]

@@ -45,7 +45,9 @@ struct SamplerParams {
     uint32_t mask_lo;       // 2^h_lo - 1
     int32_t h_lo;           // width of the low half
     uint64_t n;             // items
-    int64_t ns;             // num_samples (length of a rank's row)
+    int64_t ns;             // num_samples (length of a rank's list)
+    int64_t start;          // first list position written (resume offset)
+    int64_t row_len;        // ns - start: output slots per rank
     int64_t per_warp;       // slots per pool; pools never cross a row
     int64_t pools_per_row;  // ceil(ns / per_warp)
     int64_t pools;          // rows * pools_per_row
@@ -122,10 +124,10 @@ __global__ void __launch_bounds__(kThreads) sampler_kernel(const __grid_constant
          pool += warps) {
         const int64_t row = pool / a.pools_per_row;
         const int64_t s0 = (pool - row * a.pools_per_row) * a.per_warp;
-        const int32_t len = static_cast<int32_t>(min(a.per_warp, a.ns - s0));
+        const int32_t len = static_cast<int32_t>(min(a.per_warp, a.row_len - s0));
         const int64_t r = a.rank >= 0 ? a.rank : row;
-        int64_t* out = a.out + (a.rank >= 0 ? 0 : row * a.ns) + s0;
-        const U pos0 = static_cast<U>(r) + static_cast<U>(s0) * N;
+        int64_t* out = a.out + (a.rank >= 0 ? 0 : row * a.row_len) + s0;
+        const U pos0 = static_cast<U>(r) + static_cast<U>(a.start + s0) * N;
         if (!(a.shuffle && a.n > 1)) {
             for (int32_t o = lane; o < len; o += 32) out[o] = static_cast<int64_t>(wrap<U>(pos0 + o * N, n));
             continue;
@@ -171,16 +173,18 @@ extern "C" int64_t dist_sampler_num_samples(int64_t n_items, int32_t n_replicas,
     return drop_last ? n_items / n_replicas : (n_items + n_replicas - 1) / n_replicas;
 }
 
-extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t rank,
-                                    uint64_t seed, uint64_t epoch, int32_t shuffle, int32_t drop_last,
-                                    int64_t* out, int64_t out_capacity, int64_t* num_samples_out,
-                                    int32_t* walk_status, void* stream) {
+extern "C" int dist_sampler_indices_from(int64_t n_items, int32_t n_replicas, int32_t rank,
+                                         uint64_t seed, uint64_t epoch, int32_t shuffle, int32_t drop_last,
+                                         int64_t start, int64_t* out, int64_t out_capacity,
+                                         int64_t* num_samples_out, int32_t* walk_status, void* stream) {
     if (num_samples_out == nullptr) return DDP_ERR_INVALID_ARG;
     if (shuffle != 0 && shuffle != 1) return DDP_ERR_INVALID_ARG;
     const int64_t ns = dist_sampler_num_samples(n_items, n_replicas, drop_last);
     if (ns < 0 || rank < -1 || rank >= n_replicas || out_capacity < 0) return DDP_ERR_INVALID_ARG;
     *num_samples_out = ns;
-    const int64_t count = rank >= 0 ? ns : ns * n_replicas;
+    if (start < 0 || start > ns) return DDP_ERR_INVALID_ARG;
+    const int64_t row_len = ns - start;
+    const int64_t count = rank >= 0 ? row_len : row_len * n_replicas;
     if (out_capacity < count) return DDP_ERR_CAPACITY;
     if (count > 0 && out == nullptr) return DDP_ERR_INVALID_ARG;
     if (out != nullptr && (reinterpret_cast<uintptr_t>(out) & 7u)) return DDP_ERR_ALIGNMENT;
@@ -216,6 +220,8 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     p.mask_hi = static_cast<uint32_t>((uint64_t(1) << (bits - p.h_lo)) - 1);
     p.n = n;
     p.ns = ns;
+    p.start = start;
+    p.row_len = row_len;
     p.N = n_replicas;
     p.rank = rank;
     p.shuffle = shuffle;
@@ -233,7 +239,7 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     p.per_warp = (count + target_warps - 1) / target_warps;
     if (p.per_warp < kMinItemsPerWarp) p.per_warp = kMinItemsPerWarp;
     if (p.per_warp > (int64_t(1) << 30)) p.per_warp = int64_t(1) << 30;   // pool offsets stay int32
-    p.pools_per_row = (ns + p.per_warp - 1) / p.per_warp;
+    p.pools_per_row = (row_len + p.per_warp - 1) / p.per_warp;
     p.pools = (rank >= 0 ? 1 : n_replicas) * p.pools_per_row;
     const int64_t need = (p.pools + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const int64_t wave = static_cast<int64_t>(dev.sm_count) * per_sm;
@@ -242,4 +248,12 @@ extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t
     if (narrow) sampler_kernel<uint32_t><<<grid, kThreads, 0, s>>>(p);
     else sampler_kernel<uint64_t><<<grid, kThreads, 0, s>>>(p);
     return check_launch();
+}
+
+extern "C" int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t rank,
+                                    uint64_t seed, uint64_t epoch, int32_t shuffle, int32_t drop_last,
+                                    int64_t* out, int64_t out_capacity, int64_t* num_samples_out,
+                                    int32_t* walk_status, void* stream) {
+    return dist_sampler_indices_from(n_items, n_replicas, rank, seed, epoch, shuffle, drop_last, 0, out,
+                                     out_capacity, num_samples_out, walk_status, stream);
 }

@@ -506,6 +506,21 @@ int dist_sampler_indices(int64_t n_items, int32_t n_replicas, int32_t rank,
                          int64_t* out, int64_t out_capacity, int64_t* num_samples_out,
                          int32_t* walk_status, void* stream);
 
+/*
+ * dist_sampler_indices_from — the same lists from position `start` on
+ * (resuming an epoch part-way: each rank has already consumed the first
+ * `start` indices of its list, e.g. start = steps done × per-rank batch).
+ *   start   0 <= start <= num_samples, else DDP_ERR_INVALID_ARG
+ *   out     num_samples − start indices (rank >= 0), or all ranks rank-major
+ *           [N][num_samples − start] (rank == -1); out_capacity counts
+ *           those.  Entry k is list position start + k of dist_sampler_indices.
+ * Everything else as dist_sampler_indices (which is this call with start 0).
+ */
+int dist_sampler_indices_from(int64_t n_items, int32_t n_replicas, int32_t rank,
+                              uint64_t seed, uint64_t epoch, int32_t shuffle, int32_t drop_last,
+                              int64_t start, int64_t* out, int64_t out_capacity, int64_t* num_samples_out,
+                              int32_t* walk_status, void* stream);
+
 /* Human-readable name of a ddp_status value (static string). */
 const char* ddp_status_string(int status);
 

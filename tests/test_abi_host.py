@@ -213,6 +213,13 @@ def test_sampler_host_logic(g):
     assert f(-1, 3, 0, 0, 0, 1, 0, FAKE, 100, ctypes.addressof(ns), None, None) == g.DDP_ERR_INVALID_ARG
     assert f(2, 3, 0, 0, 0, 1, 1, None, 0, ctypes.addressof(ns), None, None) == g.DDP_OK   # n < N, drop_last
     assert ns.value == 0
+    r = lib.dist_sampler_indices_from                    # resume offset: 0 <= start <= num_samples
+    assert r(10, 3, 0, 0, 0, 1, 0, 5, FAKE, 100, ctypes.addressof(ns), None, None) == g.DDP_ERR_INVALID_ARG
+    assert r(10, 3, 0, 0, 0, 1, 0, -1, FAKE, 100, ctypes.addressof(ns), None, None) == g.DDP_ERR_INVALID_ARG
+    assert r(10, 3, 0, 0, 0, 1, 0, 1, FAKE, 2, ctypes.addressof(ns), None, None) == g.DDP_ERR_CAPACITY
+    assert r(10, 3, -1, 0, 0, 1, 0, 1, FAKE, 8, ctypes.addressof(ns), None, None) == g.DDP_ERR_CAPACITY
+    assert r(10, 3, -1, 0, 0, 1, 0, 4, None, 0, ctypes.addressof(ns), None, None) == g.DDP_OK   # nothing left
+    assert ns.value == 4
 
 
 def test_accum_clip_rejects(g):

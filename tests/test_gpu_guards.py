@@ -186,3 +186,11 @@ def test_sampler_outputs(g):
                     assert st.t.item() == 0
                     want = oracle.dist_sampler_indices(n, N, rank, 3, 1, shuffle, False).reshape(-1)
                     np.testing.assert_array_equal(out.t.cpu().numpy(), want)
+    for start in (0, 7, 20_000):
+        ns = g.dist_sampler_num_samples(100_003, 3, False)
+        out = Guarded((ns - start) * 3, torch.int64)
+        g.dist_sampler_indices_from(100_003, 3, -1, 3, 1, True, False, start, out.t)
+        sync()
+        out.check(f"sampler from {start}")
+        want = oracle.dist_sampler_indices(100_003, 3, -1, 3, 1, True, False)[:, start:].reshape(-1)
+        np.testing.assert_array_equal(out.t.cpu().numpy(), want)

@@ -69,3 +69,24 @@ def test_seed_epoch_wraparound(g):
     a = _gpu(g, 1000, 4, -1, 2 ** 64 - 1, 1, True, False)
     b = _gpu(g, 1000, 4, -1, 0, 0, True, False)
     np.testing.assert_array_equal(a, b)
+
+
+def test_resume_from_offset(g):
+    """dist_sampler_indices_from: entry k is list position start + k of the
+    full lists, for one rank and for all ranks (rank-major), every offset
+    from 0 to num_samples."""
+    for n, N in ((1_281_167, 8), (100_003, 3), (10, 4), (5, 8), (1, 1)):
+        for shuffle in (True, False):
+            full = oracle.dist_sampler_indices(n, N, -1, 9, 4, shuffle, False)
+            ns = full.shape[1]
+            for start in sorted({0, 1, ns // 2, max(ns - 1, 0), ns} & set(range(ns + 1))):
+                for rank in (-1, 0, N - 1):
+                    cnt = (ns - start) * (N if rank < 0 else 1)
+                    out = torch.full((max(cnt, 1),), -7, dtype=torch.int64, device="cuda")
+                    got_ns = g.dist_sampler_indices_from(n, N, rank, 9, 4, shuffle, False, start,
+                                                         out[:cnt] if cnt else None)
+                    sync()
+                    assert got_ns == ns
+                    want = full[:, start:] if rank < 0 else full[rank, start:]
+                    np.testing.assert_array_equal(out[:cnt].cpu().numpy(), want.reshape(-1),
+                                                  f"n={n} N={N} rank={rank} start={start} shuffle={shuffle}")
