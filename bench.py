@@ -50,7 +50,7 @@ L2_BYTES = 129 * 10 ** 6
 STEP_STREAMS = 8       # streams the headline step's bucket launches are spread over
 SYNCBN_CALLS = 10      # calls captured per graph in the SyncBN rows
 SAMPLER_CALLS = 20     # calls (epochs 1..20) captured per graph in the sampler row
-SAMPLER_WARP_INST = {"alu": 2_706_042, "fmaheavy": 2_147_028, "all": 6_238_443}
+SAMPLER_WARP_INST = {"alu": 2_712_355, "fmaheavy": 2_149_134, "all": 6_251_798}
 
 
 def parse_args():
