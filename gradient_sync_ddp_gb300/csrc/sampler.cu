@@ -31,7 +31,8 @@ constexpr int kRounds = 4;
 constexpr int kWalkCap = 4096;
 constexpr int kBlocksPerSm = 3;                    // target CTAs per SM (fewer if occupancy caps it)
 constexpr int64_t kMinItemsPerWarp = 64;
-constexpr int kWarpsPerBlock = kThreads / 32;
+constexpr int kSamplerThreads = 256;               // threads per CTA
+constexpr int kWarpsPerBlock = kSamplerThreads / 32;
 
 struct SamplerParams {
     int64_t* out;
@@ -113,14 +114,14 @@ __device__ __forceinline__ U wrap(U pos, U n) {
 // copy and stores nothing.  U is uint32_t when n <= 2^31: then every
 // position is below total < n + N < 2^32 and both halves below 2^16.
 template <typename U>
-__global__ void __launch_bounds__(kThreads) sampler_kernel(const __grid_constant__ SamplerParams a) {
+__global__ void __launch_bounds__(kSamplerThreads) sampler_kernel(const __grid_constant__ SamplerParams a) {
     constexpr bool kNarrow = sizeof(U) == 4;
     const int lane = threadIdx.x & 31;
     const unsigned lanes_below = (1u << lane) - 1u;
     const U n = static_cast<U>(a.n);
     const U N = static_cast<U>(a.N);
     const int64_t warps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
-    for (int64_t pool = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) / 32; pool < a.pools;
+    for (int64_t pool = (static_cast<int64_t>(blockIdx.x) * kSamplerThreads + threadIdx.x) / 32; pool < a.pools;
          pool += warps) {
         const int64_t row = pool / a.pools_per_row;
         const int64_t s0 = (pool - row * a.pools_per_row) * a.per_warp;
@@ -233,7 +234,7 @@ extern "C" int dist_sampler_indices_from(int64_t n_items, int32_t n_replicas, in
     int st = current_device_info(&dev);
     if (st != DDP_OK) return st;
     int per_sm = 1;
-    if ((st = resident_blocks_per_sm(kernel, kThreads, &per_sm)) != DDP_OK) return st;
+    if ((st = resident_blocks_per_sm(kernel, kSamplerThreads, &per_sm)) != DDP_OK) return st;
     const int64_t target_warps = static_cast<int64_t>(dev.sm_count) * (per_sm < kBlocksPerSm ? per_sm : kBlocksPerSm) *
                                  kWarpsPerBlock;
     p.per_warp = (count + target_warps - 1) / target_warps;
@@ -245,8 +246,8 @@ extern "C" int dist_sampler_indices_from(int64_t n_items, int32_t n_replicas, in
     const int64_t wave = static_cast<int64_t>(dev.sm_count) * per_sm;
     const int grid = static_cast<int>(need < wave ? need : wave);
     // plain launch: the status word's memset just before must complete first
-    if (narrow) sampler_kernel<uint32_t><<<grid, kThreads, 0, s>>>(p);
-    else sampler_kernel<uint64_t><<<grid, kThreads, 0, s>>>(p);
+    if (narrow) sampler_kernel<uint32_t><<<grid, kSamplerThreads, 0, s>>>(p);
+    else sampler_kernel<uint64_t><<<grid, kSamplerThreads, 0, s>>>(p);
     return check_launch();
 }
 
