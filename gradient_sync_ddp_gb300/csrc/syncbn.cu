@@ -60,6 +60,7 @@ constexpr int kTargetCtas = 2048;        // stats CTAs aimed for (about two wave
 constexpr int64_t kMaxPartials = 65536;  // C*S bound: fp32 partials stay <= 512 KiB
 constexpr int kRunElems = 2048;          // channels per group: G*H*W <= this (G >= 1)
 constexpr int kStageBytes = 32768;       // shared staging buffer per CTA (staged group kernel)
+constexpr int kPlaneVecsPerThread = 24;  // plane statistics: slices sized for this many vectors per thread
 constexpr int kApplyWaves = 8;           // apply grid: at most this many waves of resident CTAs
 constexpr int kApplyVecs = 8;            // apply grid: at least this many 16-byte vectors per thread
 
@@ -829,6 +830,16 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
         sp.slot_bytes = 0;
         sp.R = 0;
         sp.S = slices_for(C, P, C);
+        if (sp.kind == kPlaneVec) {
+            // slices by work per thread, about kPlaneVecsPerThread 16-byte vectors each (measured on
+            // 8 x [32,C,56|28,..] bf16: 24 beat the fixed CTA target, 8-12 and 32 were slower)
+            const int64_t vecs = static_cast<int64_t>(P) * (HW / W);
+            int64_t S = vecs / (static_cast<int64_t>(kThreads) * kPlaneVecsPerThread);
+            if (S > P) S = P;
+            if (S > kMaxPartials / C) S = kMaxPartials / C;
+            if (S < 1) S = 1;
+            sp.S = static_cast<int>(S);
+        }
     }
     return sp;
 }
