@@ -633,6 +633,26 @@ def bench_rows(g, torch, dev, peak, peak_kind):
                                        "frac": nbytes / ms / 1e6 / peak, "launches": 5}
     del acc, gavg, theta, buf
 
+    # the ResNet-50 step in the other reduction orders (ring chunks, pairwise tree), same schedule
+    num_r = workloads.numels(workloads.resnet50_layout())
+    plan_r = g.ddp_plan_buckets(num_r, 4, 25 << 20)
+    reps_r = [workloads.device_normal((plan_r["total_elems"],), 0.0, 0.01, workloads.seed_for(2, r), device=dev)
+              for r in range(N_REPLICAS)]
+    out_r = torch.empty(plan_r["total_elems"], device=dev)
+    pool_r = [torch.cuda.Stream(device=dev) for _ in range(len(plan_r["buckets"]))]
+    nbytes = sum((N_REPLICAS + 1) * 4 * b[1] for b in plan_r["buckets"])
+    for name, flag in (("ring", g.FLAG_RING_ORDER), ("tree", g.FLAG_TREE_ORDER)):
+        def ordered(flag=flag):
+            _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_mean(
+                [x[off:off + n] for x in reps_r], out_r[off:off + n], flags=flag)
+                for off, n, _, _ in plan_r["buckets"]], pool_r)
+        ms = _time_launches(torch, ordered, 200, side)
+        rows[f"mean_{name}_order_resnet50"] = {
+            "workload": f"ResNet-50 step (5 x 25 MiB buckets, 8 fp32 replicas), {name}-order reduction",
+            "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+            "launches": len(plan_r["buckets"])}
+    del reps_r, out_r
+
     # SyncBN, 4 shapes
     for C, H, W in workloads.SYNCBN_SHAPES:
         B = workloads.SYNCBN_BATCH
