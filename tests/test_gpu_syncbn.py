@@ -95,15 +95,18 @@ def test_small_shapes(g, shape, io):
         _check_y(ys[r], y_w[r], f"{shape} {io} y[{r}]")
 
 
-def test_in_place_and_defaults(g):
-    n, B, C, H, W = 4, 2, 6, 5, 5
+@pytest.mark.parametrize("shape", [(4, 2, 6, 5, 5), (4, 3, 6, 8, 16), (2, 4, 3, 28, 28)])
+def test_in_place_and_defaults(g, shape):
+    """y written over x, for unaligned (5x5) and aligned (8x16, 28x28)
+    planes: the apply reads x through the coherent path when they alias."""
+    n, B, C, H, W = shape
     xs = workloads.syncbn_input(4, n, B, C, H, W)
     xs_dev = [dev_bf16(x) for x in xs]
     mean, invstd = _run(g, xs_dev, xs_dev, C)
     m_w, s_w, y_w = oracle.syncbn(xs, 1e-5)
-    _check_stats(mean, invstd, m_w, s_w, "in place")
+    _check_stats(mean, invstd, m_w, s_w, f"in place {shape}")
     for r in range(n):
-        _check_y(xs_dev[r], y_w[r], f"in place y[{r}]")
+        _check_y(xs_dev[r], y_w[r], f"in place {shape} y[{r}]")
 
 
 def test_constant_channel(g):
