@@ -7,7 +7,8 @@
  * library averages them bucket by bucket (optionally fused with the bf16 ->
  * fp32 widen and an SGD step), merges SyncBatchNorm statistics across the
  * replicas and applies the normalisation, and produces DistributedSampler
- * index lists.
+ * index lists; a host-side tracker tells when a bucket's gradients are all
+ * ready.
  *
  * Sources (web pages, cited by title and section):
  *   [TR24] Tech-Renaissance, "(24) NCCL通信与分布式数据并行"
@@ -24,7 +25,10 @@
  *     during the call only; their contents are copied into the kernel's
  *     launch parameters, so the calls may be captured into a CUDA Graph.
  *   - Asynchrony: work is enqueued on `stream` and the call returns at once.
- *     Results are valid once the stream has reached that point.
+ *     Results are valid once the stream has reached that point.  Calls on
+ *     disjoint buffers (e.g. different buckets) may be issued on different
+ *     streams: the GPU then starts one launch on the SMs the previous one
+ *     frees instead of after its whole grid.
  *   - Errors: every entry point returns an int status (ddp_status below) and
  *     never throws or aborts.  Arguments are validated on the host before any
  *     CUDA call; an invalid call enqueues nothing and leaves every buffer
