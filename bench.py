@@ -235,10 +235,35 @@ def cpu_oracle_rate(plan, budget_s: float, seed_base: int = 0):
             break
     dt = time.perf_counter() - t0
     nbytes = (N_REPLICAS + 1) * 4 * elems * passes
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    line = {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"first {k:,} elements of each of the {len(plan['buckets'])} buckets x {N_REPLICAS} "
                       f"replicas ({elems:,} elements per pass), {passes} passes in {dt:.1f} s, numpy "
                       f"single-threaded on {os.cpu_count()} host cores"}
+    line["c_oracle"] = c_oracle_rates(data)
+    return line
+
+
+def c_oracle_rates(data, budget_s: float = 3.0):
+    """Context beside the numpy figure: the plain-C restatement of the same
+    average (oracle/mean_ref.c, pinned bit-exact to the numpy oracle) on the
+    same sample, single-threaded and split over the host's threads."""
+    from oracle import cref
+    if not cref.available():
+        return None
+    out = {}
+    elems = sum(len(d[0]) for d in data)
+    for name, threaded in (("single_thread", False), ("threads", True)):
+        passes, t0 = 0, time.perf_counter()
+        while True:
+            for d in data:
+                cref.grad_mean_c(d, threaded=threaded)
+            passes += 1
+            if time.perf_counter() - t0 >= budget_s or passes >= 1000:
+                break
+        dt = time.perf_counter() - t0
+        out[name + "_GBps"] = (N_REPLICAS + 1) * 4 * elems * passes / dt / 1e9
+    out["threads"] = cref.threads()
+    return out
 
 
 # ----------------------------------------------------------------------------- reference arm
