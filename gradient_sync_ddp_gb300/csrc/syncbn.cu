@@ -95,6 +95,46 @@ __device__ __forceinline__ float shared_elem(const unsigned char* p, int e) {
     else return reinterpret_cast<const float*>(p)[e];
 }
 
+// Two fp32 values in one 64-bit register pair, for the packed f32x2
+// arithmetic of the sm_100 family: one instruction does both lanes, each
+// rounded to nearest even exactly as the scalar add, subtract or fused
+// multiply-add would.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Elements (2j, 2j + 1) of a 16-byte vector of 8 bf16 or 4 fp32 values, as an fp32 pair.
+template <bool BF16>
+__device__ __forceinline__ uint64_t vec_pair(const uint4& v, int j) {
+    if constexpr (BF16) {
+        const uint32_t w = j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+        return f2_pack(bf16_lo(w), bf16_hi(w));
+    } else {
+        return j == 0 ? f2_pack(__uint_as_float(v.x), __uint_as_float(v.y))
+                      : f2_pack(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+}
+
 // Samples [p0, p1) of slice s: p_k = floor(P*k/S) with P = n*batch.
 __device__ __forceinline__ void slice_bounds(const BnParams& a, int s, int& p0, int& p1) {
     const int P = a.n * a.batch;
@@ -239,13 +279,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 template <bool BF16>
 __device__ __forceinline__ void sum_range(const unsigned char* buf, uint32_t byte0, uint32_t count, float K,
                                           float& acc_s, float& acc_q) {
-    float s0 = 0.0f, s1 = 0.0f, q0 = 0.0f, q1 = 0.0f;
+    // element pairs in packed f32x2 accumulators, a ragged first or last element in scalar ones
+    float s0 = 0.0f, q0 = 0.0f;
+    const uint64_t K2 = f2_pack(K, K);
+    uint64_t s2 = f2_pack(0.0f, 0.0f), q2 = s2;
+    auto add_pair = [&](float lo, float hi) {
+        const uint64_t d = f2_sub(f2_pack(lo, hi), K2);
+        s2 = f2_add(s2, d);
+        q2 = f2_fma(d, d, q2);
+    };
     if constexpr (BF16) {
         const uint32_t* w = reinterpret_cast<const uint32_t*>(buf);
         uint32_t h = byte0 >> 1;
         const uint32_t hend = h + count;
         if ((h & 1u) && h < hend) {                          // odd start: high half of a word
-            const float d = __fsub_rn(__uint_as_float(w[h >> 1] & 0xFFFF0000u), K);
+            const float d = __fsub_rn(bf16_hi(w[h >> 1]), K);
             s0 += d;
             q0 = fmaf(d, d, q0);
             ++h;
@@ -255,26 +303,14 @@ __device__ __forceinline__ void sum_range(const unsigned char* buf, uint32_t byt
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[i] = w[(h >> 1) + i];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float dl = __fsub_rn(__uint_as_float(v[i] << 16), K);
-                const float dh = __fsub_rn(__uint_as_float(v[i] & 0xFFFF0000u), K);
-                s0 += dl;
-                q0 = fmaf(dl, dl, q0);
-                s1 += dh;
-                q1 = fmaf(dh, dh, q1);
-            }
+            for (int i = 0; i < 4; ++i) add_pair(bf16_lo(v[i]), bf16_hi(v[i]));
         }
         for (; h + 2 <= hend; h += 2) {
             const uint32_t v = w[h >> 1];
-            const float dl = __fsub_rn(__uint_as_float(v << 16), K);
-            const float dh = __fsub_rn(__uint_as_float(v & 0xFFFF0000u), K);
-            s0 += dl;
-            q0 = fmaf(dl, dl, q0);
-            s1 += dh;
-            q1 = fmaf(dh, dh, q1);
+            add_pair(bf16_lo(v), bf16_hi(v));
         }
         if (h < hend) {                                      // last element: low half of a word
-            const float d = __fsub_rn(__uint_as_float(w[h >> 1] << 16), K);
+            const float d = __fsub_rn(bf16_lo(w[h >> 1]), K);
             s0 += d;
             q0 = fmaf(d, d, q0);
         }
@@ -282,14 +318,8 @@ __device__ __forceinline__ void sum_range(const unsigned char* buf, uint32_t byt
         const float* f = reinterpret_cast<const float*>(buf) + (byte0 >> 2);
         uint32_t i = 0;
         for (; i + 4 <= count; i += 4) {
-#pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-                const float da = __fsub_rn(f[i + u], K), db = __fsub_rn(f[i + u + 1], K);
-                s0 += da;
-                q0 = fmaf(da, da, q0);
-                s1 += db;
-                q1 = fmaf(db, db, q1);
-            }
+            add_pair(f[i], f[i + 1]);
+            add_pair(f[i + 2], f[i + 3]);
         }
         for (; i < count; ++i) {
             const float d = __fsub_rn(f[i], K);
@@ -297,8 +327,11 @@ __device__ __forceinline__ void sum_range(const unsigned char* buf, uint32_t byt
             q0 = fmaf(d, d, q0);
         }
     }
-    acc_s += s0 + s1;
-    acc_q += q0 + q1;
+    float sl, sh, ql, qh;
+    f2_unpack(s2, sl, sh);
+    f2_unpack(q2, ql, qh);
+    acc_s += (s0 + sl) + sh;
+    acc_q += (q0 + ql) + qh;
 }
 
 template <bool BF16, int CPL>
@@ -459,7 +492,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
 constexpr int kChunkVecs = 64;
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_constant__ BnParams a) {
+__global__ void __launch_bounds__(kThreads, 5) bn_stats_plane_kernel(const __grid_constant__ BnParams a) {
     constexpr int W = BF16 ? 8 : 4;    // elements per 16-byte access
     constexpr int ESZ = BF16 ? 2 : 4;
     constexpr int kWarps = kThreads / 32;
@@ -473,10 +506,13 @@ __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_c
     pdl_enter();
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
     // one (Σd, Σd²) pair per element position of the vector: each sums one element per vector (as
-    // many terms as a per-vector total would), at one add and one fused multiply-add per element
-    float ps[W], pq[W];
+    // many terms as a per-vector total would), at one add and one fused multiply-add per element,
+    // done two positions per packed f32x2 instruction
+    constexpr int NP = W / 2;
+    const uint64_t K2 = f2_pack(K, K);
+    uint64_t s2[NP], q2[NP];
 #pragma unroll
-    for (int k = 0; k < W; ++k) ps[k] = pq[k] = 0.0f;
+    for (int j = 0; j < NP; ++j) s2[j] = q2[j] = f2_pack(0.0f, 0.0f);
     for (uint32_t ch0 = warp; ch0 < total; ch0 += 2 * kWarps) {
         uint4 raw[2][2];
         bool ok[2][2];
@@ -503,12 +539,18 @@ __global__ void __launch_bounds__(kThreads) bn_stats_plane_kernel(const __grid_c
             for (int u = 0; u < 2; ++u) {
                 if (!ok[i][u]) continue;
 #pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    const float d = __fsub_rn(vec_elem<BF16>(raw[i][u], k), K);
-                    ps[k] += d;
-                    pq[k] = fmaf(d, d, pq[k]);
+                for (int j = 0; j < NP; ++j) {
+                    const uint64_t d = f2_sub(vec_pair<BF16>(raw[i][u], j), K2);
+                    s2[j] = f2_add(s2[j], d);
+                    q2[j] = f2_fma(d, d, q2[j]);
                 }
             }
+    }
+    float ps[W], pq[W];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+        f2_unpack(s2[j], ps[2 * j], ps[2 * j + 1]);
+        f2_unpack(q2[j], pq[2 * j], pq[2 * j + 1]);
     }
 #pragma unroll
     for (int w = W; w > 1; w >>= 1)
@@ -606,12 +648,22 @@ __global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_co
     const float m_hi = static_cast<float>(mean);
     a.mean_out[cc] = m_hi;
     a.invstd_out[cc] = invstd;
-    a.coef[cc] = make_float4(m_hi, static_cast<float>(mean - static_cast<double>(m_hi)), invstd * gc, bc);
+    // y = (x − mean)·scale + β = (x − m_hi)·scale + (β − m_lo·scale): the low part of the mean
+    // goes into the shift (fp64, rounded once), so x − m_hi is the apply's only subtraction
+    const float scale = invstd * gc;
+    const double m_lo = mean - static_cast<double>(m_hi);
+    a.coef[cc] = make_float4(m_hi, scale, static_cast<float>(static_cast<double>(bc) - m_lo * static_cast<double>(scale)),
+                             0.0f);
 }
 
-// ((x − m_hi) − m_lo)·scale + β with k = (m_hi, m_lo, scale, β)
+// (x − m_hi)·scale + shift with k = (m_hi, scale, shift, unused)
 __device__ __forceinline__ float normalize(float x, float4 k) {
-    return fmaf(__fsub_rn(__fsub_rn(x, k.x), k.y), k.z, k.w);
+    return fmaf(__fsub_rn(x, k.x), k.y, k.z);
+}
+
+// The same for elements (2j, 2j + 1) of a pair, with each element's coefficients
+__device__ __forceinline__ uint64_t normalize2(uint64_t x2, const float4& ka, const float4& kb) {
+    return f2_fma(f2_sub(x2, f2_pack(ka.x, kb.x)), f2_pack(ka.y, kb.y), f2_pack(ka.z, kb.z));
 }
 
 __device__ __forceinline__ uint32_t channel_of(uint32_t e, const BnParams& a) {
@@ -649,22 +701,15 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
             const uint32_t v = v0 + u * stride;
             if (v >= nvec) continue;
             const uint32_t e0 = v * 8;
-            float xv[8];
-            if constexpr (BF16_IN) {
+            uint64_t xv[4];                                 // element pairs (2j, 2j + 1)
 #pragma unroll
-                for (int k = 0; k < 8; ++k) xv[k] = vec_elem<true>(raw[u][0], k);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    xv[k] = vec_elem<false>(raw[u][0], k);
-                    xv[4 + k] = vec_elem<false>(raw[u][1], k);
-                }
-            }
-            float yv[8];
+            for (int j = 0; j < 4; ++j)
+                xv[j] = BF16_IN ? vec_pair<true>(raw[u][0], j) : vec_pair<false>(raw[u][j >> 1], j & 1);
+            uint64_t yv2[4];
             if constexpr (CMODE == 0) {
                 const float4 k4 = __ldg(a.coef + channel_of(e0, a));
 #pragma unroll
-                for (int k = 0; k < 8; ++k) yv[k] = normalize(xv[k], k4);
+                for (int j = 0; j < 4; ++j) yv2[j] = normalize2(xv[j], k4, k4);
             } else if constexpr (CMODE == 1) {
                 const uint32_t pl = fdiv(e0, a.div_hw);
                 const uint32_t cross = static_cast<uint32_t>(a.HW) - (e0 - pl * static_cast<uint32_t>(a.HW));
@@ -672,11 +717,18 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
                 const float4 k0 = __ldg(a.coef + c0);
                 const float4 k1 = cross < 8 ? __ldg(a.coef + (c0 + 1 == static_cast<uint32_t>(a.C) ? 0 : c0 + 1)) : k0;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) yv[k] = normalize(xv[k], static_cast<uint32_t>(k) < cross ? k0 : k1);
+                for (int j = 0; j < 4; ++j)
+                    yv2[j] = normalize2(xv[j], static_cast<uint32_t>(2 * j) < cross ? k0 : k1,
+                                        static_cast<uint32_t>(2 * j + 1) < cross ? k0 : k1);
             } else {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) yv[k] = normalize(xv[k], __ldg(a.coef + channel_of(e0 + k, a)));
+                for (int j = 0; j < 4; ++j)
+                    yv2[j] = normalize2(xv[j], __ldg(a.coef + channel_of(e0 + 2 * j, a)),
+                                        __ldg(a.coef + channel_of(e0 + 2 * j + 1, a)));
             }
+            float yv[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) f2_unpack(yv2[j], yv[2 * j], yv[2 * j + 1]);
             if constexpr (BF16_OUT) {
                 st16(y + static_cast<int64_t>(e0) * OSZ,
                      make_uint4(pack_bf16x2(yv[0], yv[1]), pack_bf16x2(yv[2], yv[3]), pack_bf16x2(yv[4], yv[5]),
