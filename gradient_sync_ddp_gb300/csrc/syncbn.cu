@@ -237,14 +237,17 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
 // an mbarrier).  Only where the replica buffer ends inside a block is the
 // run's end read with plain loads.  A tile is up to kBulkRuns runs; two
 // tile buffers alternate, so the copy of tile t+2 runs while tile t+1 is
-// summed.  Warp w sums run w of the tile; within a run, lane l owns a
+// summed.  Tiles stay small (at most 4 runs of <= 8 KiB) so that 6 CTAs fit
+// per SM: on 8 x [32, 2048, 7, 7] bf16, 4-5 runs per tile (6 CTAs per SM)
+// beat 8 runs (4 CTAs per SM) by 3 %, and 2-3 runs or two waves of CTAs
+// were slower.  Warp w sums run w of the tile; within a run, lane l owns a
 // contiguous range of one channel's plane (G >= 32: whole planes of channels
 // l, l+32, ...; G < 32: 32/G lanes split each plane), so every element it
 // reads belongs to its channel and needs no mask.  Each wait for a copy is
 // bounded (about a second of globaltimer): on expiry the CTA writes NaN
 // partials for its channels, which makes the statistics NaN, instead of
 // waiting on.
-constexpr int kBulkRuns = kThreads / 32;   // runs per tile: one per warp
+constexpr int kBulkRuns = 4;             // runs per tile
 constexpr int kBulkBufMax = 32768;        // bytes per tile buffer at most
 constexpr uint64_t kCopyWaitNs = 1000000000ull;
 
