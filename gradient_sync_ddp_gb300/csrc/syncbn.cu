@@ -15,7 +15,8 @@
 //      sample and channel):
 //        plane kernel — H*W a multiple of the 16-byte vector (56x56, 28x28):
 //          CTA (c, s) streams its planes with 16-byte loads, a warp at a
-//          time over 64-vector chunks of one plane.
+//          time over 64-vector chunks of one plane, two element positions
+//          per packed f32x2 instruction.
 //        bulk-staged kernel — unaligned planes at least one vector long
 //          (7x7, 14x14, 3x3): a CTA owns G consecutive channels (G*H*W about
 //          2K elements) and a slice of the samples; for one sample those G
@@ -36,14 +37,16 @@
 //      float-float (fp32 pairs), then one thread per channel finalises: in
 //      fp64, with m' = Σd/M, mean = K_c + m' and var = Σd²/M − m'² (the same
 //      S/M and Q/M − mean² up to rounding); in fp32, invstd =
-//      1/sqrt(var + eps) with IEEE-rounded sqrt and divide.  It stores per
-//      channel (m_hi, m_lo, scale, β) where m_hi + m_lo is the mean as an
-//      fp32 pair and scale = invstd·γ.
-//   3. apply  — y = ((x − m_hi) − m_lo)·scale + β over every replica, 16-byte
-//      vectors in and out, the channel computed once per 8-element vector.
-//      x − m_hi is exact when x is near the mean (Sterbenz), so no
-//      cancellation error is amplified by a large invstd (the form
-//      x·scale + (β − mean·scale) would lose it).
+//      1/sqrt(var + eps) with IEEE-rounded sqrt and divide.  With the mean
+//      split into an fp32 pair m_hi + m_lo and scale = invstd·γ, it stores
+//      per channel (m_hi, scale, shift), shift = β − m_lo·scale formed in
+//      fp64 and rounded once.
+//   3. apply  — y = (x − m_hi)·scale + shift over every replica, 16-byte
+//      vectors in and out, the channel computed once per 8-element vector,
+//      element pairs in packed f32x2 arithmetic.  x − m_hi is exact when x
+//      is near the mean (Sterbenz), so no cancellation error is amplified
+//      by a large invstd; only the mean's tiny low part goes into the shift
+//      (the form x·scale + (β − mean·scale) would lose that protection).
 // Traffic: x is read twice and y written once (2+2+2 bytes per bf16 element).
 #include <cstdint>
 #include <map>
@@ -72,7 +75,7 @@ struct BnParams {
     float* mean_out;
     float* invstd_out;
     float2* partial;    // [C][S] (Σd, Σd²) per channel and slice
-    float4* coef;       // [C] (m_hi, m_lo, scale, beta)
+    float4* coef;       // [C] (m_hi, scale, shift, unused)
     FastDiv div_unit;   // plane kernel: accesses per plane; group kernel: 16-byte vectors per staging slot
     FastDiv div_batch;  // batch
     FastDiv div_hw;     // H*W
