@@ -378,9 +378,10 @@ size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int3
  *     y_r = (x_r − mean)·invstd·γ + β
  * Sums are shifted by each channel's first element (so Q/M − mean² does
  * not cancel when |mean| >> std); threads accumulate a few hundred
- * elements in fp32, each CTA combines its threads in fp64 and stores one
- * fp32 partial per channel, and the partials are merged in fp64; the apply
- * runs in fp32.
+ * elements in fp32, each CTA combines its threads in float-float (pairs of
+ * fp32) and stores one fp32 partial per channel and slice of the samples,
+ * and a merge kernel sums the partials in float-float and finalises in
+ * fp64; the apply runs in fp32.
  *
  *   x            host array of n_replicas device pointers, each
  *                [batch, C, H, W] NCHW contiguous, in_dtype elements
