@@ -61,6 +61,10 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-rows", action="store_true", help="skip the SGD / SyncBN / sampler rows")
+    p.add_argument("--rows", default=None,
+                   help="comma-separated subset of the side-row groups to run: gpt2 (SGD, SGD with the bf16 copy, "
+                        "bf16 average), accum (accumulation, clipped step), orders (ring and tree order), syncbn, "
+                        "sampler, sweep; default all")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     return p.parse_args()
@@ -487,7 +491,8 @@ def run_ours(args, world, rank, local):
     rows = None
     if rank == 0 and world == 1 and not args.no_rows:
         del host_reps, host_out
-        rows = bench_rows(g, torch, dev, peak, peak_kind)
+        only = None if args.rows is None else {r.strip() for r in args.rows.split(",") if r.strip()}
+        rows = bench_rows(g, torch, dev, peak, peak_kind, only)
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or world > 1 else cpu_oracle_rate(plan, args.cpu_seconds)
@@ -567,7 +572,7 @@ def _fan_out(torch, calls, streams):
         cur.wait_stream(st)
 
 
-def bench_rows(g, torch, dev, peak, peak_kind):
+def bench_rows(g, torch, dev, peak, peak_kind, only=None):
     """The other rows of the hot path, each on its own workload (not part of
     the headline value): fused SGD on GPT-2 small, SyncBN on the four
     activation shapes, the ImageNet-size sampler, and the bf16 average."""
@@ -576,185 +581,195 @@ def bench_rows(g, torch, dev, peak, peak_kind):
     pool = [torch.cuda.Stream(device=dev) for _ in range(2)]   # the two GPT-2 buckets are disjoint
     rows = {}
 
-    # fused SGD, GPT-2 small DEEP/FIRST, bf16 grads, momentum 0.9, wd 1e-4
-    layout, first = workloads.gpt2_small_layout()
+    def want(group):
+        return only is None or group in only
+
+    layout, first = workloads.gpt2_small_layout()      # GPT-2 small parameter list (gpt2 and accum rows)
     num = workloads.numels(layout)
-    plan = g.ddp_plan_buckets(num, 2, 0, g.PLAN_DEEP_FIRST, first)
-    total = plan["total_elems"]
-    reps = [workloads.device_normal((total,), 0.0, 0.01, workloads.seed_for(3, r), device=dev,
-                                    dtype=torch.bfloat16) for r in range(N_REPLICAS)]
-    theta = workloads.device_normal((total,), 0.0, 0.02, workloads.seed_for(3, 99), device=dev)
-    buf = torch.zeros(total, device=dev)
 
-    def sgd_step():
-        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_sgd(
-            [x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4)
-            for off, n, _, _ in plan["buckets"]], pool)
-    ms = _time_launches(torch, sgd_step, 50, side)
-    nbytes = sum((2 * N_REPLICAS + 16) * b[1] for b in plan["buckets"])
-    rows["sgd_gpt2_small"] = {"workload": "GPT-2 small (124,439,808 params), 8 bf16 replicas, DEEP/FIRST buckets, "
-                                          "SGD momentum 0.9 wd 1e-4", "ms": ms, "bytes": nbytes,
-                              "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+    if want("gpt2"):
+        # fused SGD, GPT-2 small DEEP/FIRST, bf16 grads, momentum 0.9, wd 1e-4
+        plan = g.ddp_plan_buckets(num, 2, 0, g.PLAN_DEEP_FIRST, first)
+        total = plan["total_elems"]
+        reps = [workloads.device_normal((total,), 0.0, 0.01, workloads.seed_for(3, r), device=dev,
+                                        dtype=torch.bfloat16) for r in range(N_REPLICAS)]
+        theta = workloads.device_normal((total,), 0.0, 0.02, workloads.seed_for(3, 99), device=dev)
+        buf = torch.zeros(total, device=dev)
 
-    # the same step also writing the bf16 compute copy of θ
-    low = torch.empty(total, dtype=torch.bfloat16, device=dev)
+        def sgd_step():
+            _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_sgd(
+                [x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4)
+                for off, n, _, _ in plan["buckets"]], pool)
+        ms = _time_launches(torch, sgd_step, 50, side)
+        nbytes = sum((2 * N_REPLICAS + 16) * b[1] for b in plan["buckets"])
+        rows["sgd_gpt2_small"] = {"workload": "GPT-2 small (124,439,808 params), 8 bf16 replicas, DEEP/FIRST buckets, "
+                                              "SGD momentum 0.9 wd 1e-4", "ms": ms, "bytes": nbytes,
+                                  "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
 
-    def sgd_cast_step():
-        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_sgd_cast(
-            [x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, low[off:off + n])
-            for off, n, _, _ in plan["buckets"]], pool)
-    ms = _time_launches(torch, sgd_cast_step, 50, side)
-    nbytes = sum((2 * N_REPLICAS + 18) * b[1] for b in plan["buckets"])
-    rows["sgd_cast_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, SGD momentum 0.9 wd 1e-4 plus the "
-                                               "bf16 copy of θ", "ms": ms, "bytes": nbytes,
-                                   "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
-    del low
+        # the same step also writing the bf16 compute copy of θ
+        low = torch.empty(total, dtype=torch.bfloat16, device=dev)
 
-    # bf16 -> fp32 average of the same buckets
-    outb = torch.empty(total, device=dev)
+        def sgd_cast_step():
+            _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_sgd_cast(
+                [x[off:off + n] for x in reps], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, low[off:off + n])
+                for off, n, _, _ in plan["buckets"]], pool)
+        ms = _time_launches(torch, sgd_cast_step, 50, side)
+        nbytes = sum((2 * N_REPLICAS + 18) * b[1] for b in plan["buckets"])
+        rows["sgd_cast_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, SGD momentum 0.9 wd 1e-4 plus the "
+                                                   "bf16 copy of θ", "ms": ms, "bytes": nbytes,
+                                       "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+        del low
 
-    def mean_bf16():
-        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps],
-                                                                          outb[off:off + n])
-                         for off, n, _, _ in plan["buckets"]], pool)
-    ms = _time_launches(torch, mean_bf16, 50, side)
-    nbytes = sum((2 * N_REPLICAS + 4) * b[1] for b in plan["buckets"])
-    rows["mean_bf16_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, DEEP/FIRST, average to fp32",
-                                    "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
-                                    "frac": nbytes / ms / 1e6 / peak, "launches": 2}
-    del reps, theta, buf, outb
+        # bf16 -> fp32 average of the same buckets
+        outb = torch.empty(total, device=dev)
 
-    # gradient accumulation (no_sync micro-step) and the clipped final step, GPT-2 small, fp32 accumulators
-    plan4 = g.ddp_plan_buckets(num, 4, 0, g.PLAN_DEEP_FIRST, first)
-    total4 = plan4["total_elems"]
-    acc = [torch.zeros(total4, device=dev) for _ in range(N_REPLICAS)]
-    micro = [workloads.device_normal((total4,), 0.0, 0.01, workloads.seed_for(3, r) + 50, device=dev,
-                                     dtype=torch.bfloat16) for r in range(N_REPLICAS)]
-    ms = _time_launches(torch, lambda: g.ddp_bucket_accumulate(micro, acc), 20, side)
-    nbytes = (2 + 8) * N_REPLICAS * total4
-    rows["accumulate_gpt2_small"] = {"workload": "GPT-2 small, 8 replicas, bf16 micro-step gradient added into "
-                                                 "fp32 accumulators (no_sync)", "ms": ms, "bytes": nbytes,
-                                     "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 1}
-    del micro
-    gavg = torch.empty(total4, device=dev)
-    theta = workloads.device_normal((total4,), 0.0, 0.02, workloads.seed_for(3, 99), device=dev)
-    buf = torch.zeros(total4, device=dev)
-    ws = torch.empty(g.ddp_norm_workspace_bytes(len(plan4["buckets"])), dtype=torch.uint8, device=dev)
-    coef = torch.empty(1, device=dev)
+        def mean_bf16():
+            _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_mean([x[off:off + n] for x in reps],
+                                                                              outb[off:off + n])
+                             for off, n, _, _ in plan["buckets"]], pool)
+        ms = _time_launches(torch, mean_bf16, 50, side)
+        nbytes = sum((2 * N_REPLICAS + 4) * b[1] for b in plan["buckets"])
+        rows["mean_bf16_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, DEEP/FIRST, average to fp32",
+                                        "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
+                                        "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+        del reps, theta, buf, outb
 
-    def clipped_step():
-        _fan_out(torch, [lambda b=b, off=off, n=n: g.ddp_bucket_allreduce_mean_norm(
-            [x[off:off + n] for x in acc], gavg[off:off + n], ws, b)
-            for b, (off, n, _, _) in enumerate(plan4["buckets"])], pool)
-        g.ddp_grad_norm_finalize(ws, len(plan4["buckets"]), 1.0, None, coef, None)
-        _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_sgd(
-            gavg[off:off + n], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, grad_scale=coef)
-            for off, n, _, _ in plan4["buckets"]], pool)
-    ms = _time_launches(torch, clipped_step, 20, side)
-    nbytes = sum(((N_REPLICAS + 1) * 4 + 20) * b[1] for b in plan4["buckets"])
-    rows["clipped_step_gpt2_small"] = {"workload": "GPT-2 small, 8 fp32 accumulated replicas: average with norm "
-                                                   "side output, clip to 1.0, SGD momentum 0.9 wd 1e-4",
-                                       "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
-                                       "frac": nbytes / ms / 1e6 / peak, "launches": 5}
-    del acc, gavg, theta, buf
+    if want("accum"):
+        # gradient accumulation (no_sync micro-step) and the clipped final step, GPT-2 small, fp32 accumulators
+        plan4 = g.ddp_plan_buckets(num, 4, 0, g.PLAN_DEEP_FIRST, first)
+        total4 = plan4["total_elems"]
+        acc = [torch.zeros(total4, device=dev) for _ in range(N_REPLICAS)]
+        micro = [workloads.device_normal((total4,), 0.0, 0.01, workloads.seed_for(3, r) + 50, device=dev,
+                                         dtype=torch.bfloat16) for r in range(N_REPLICAS)]
+        ms = _time_launches(torch, lambda: g.ddp_bucket_accumulate(micro, acc), 20, side)
+        nbytes = (2 + 8) * N_REPLICAS * total4
+        rows["accumulate_gpt2_small"] = {"workload": "GPT-2 small, 8 replicas, bf16 micro-step gradient added into "
+                                                     "fp32 accumulators (no_sync)", "ms": ms, "bytes": nbytes,
+                                         "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 1}
+        del micro
+        gavg = torch.empty(total4, device=dev)
+        theta = workloads.device_normal((total4,), 0.0, 0.02, workloads.seed_for(3, 99), device=dev)
+        buf = torch.zeros(total4, device=dev)
+        ws = torch.empty(g.ddp_norm_workspace_bytes(len(plan4["buckets"])), dtype=torch.uint8, device=dev)
+        coef = torch.empty(1, device=dev)
 
-    # the ResNet-50 step in the other reduction orders (ring chunks, pairwise tree), same schedule
-    num_r = workloads.numels(workloads.resnet50_layout())
-    plan_r = g.ddp_plan_buckets(num_r, 4, 25 << 20)
-    reps_r = [workloads.device_normal((plan_r["total_elems"],), 0.0, 0.01, workloads.seed_for(2, r), device=dev)
-              for r in range(N_REPLICAS)]
-    out_r = torch.empty(plan_r["total_elems"], device=dev)
-    pool_r = [torch.cuda.Stream(device=dev) for _ in range(len(plan_r["buckets"]))]
-    nbytes = sum((N_REPLICAS + 1) * 4 * b[1] for b in plan_r["buckets"])
-    for name, flag in (("ring", g.FLAG_RING_ORDER), ("tree", g.FLAG_TREE_ORDER)):
-        def ordered(flag=flag):
-            _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_mean(
-                [x[off:off + n] for x in reps_r], out_r[off:off + n], flags=flag)
-                for off, n, _, _ in plan_r["buckets"]], pool_r)
-        ms = _time_launches(torch, ordered, 200, side)
-        rows[f"mean_{name}_order_resnet50"] = {
-            "workload": f"ResNet-50 step (5 x 25 MiB buckets, 8 fp32 replicas), {name}-order reduction",
-            "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-            "launches": len(plan_r["buckets"])}
-    del reps_r, out_r
+        def clipped_step():
+            _fan_out(torch, [lambda b=b, off=off, n=n: g.ddp_bucket_allreduce_mean_norm(
+                [x[off:off + n] for x in acc], gavg[off:off + n], ws, b)
+                for b, (off, n, _, _) in enumerate(plan4["buckets"])], pool)
+            g.ddp_grad_norm_finalize(ws, len(plan4["buckets"]), 1.0, None, coef, None)
+            _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_sgd(
+                gavg[off:off + n], theta[off:off + n], buf[off:off + n], 0.1, 0.9, 1e-4, grad_scale=coef)
+                for off, n, _, _ in plan4["buckets"]], pool)
+        ms = _time_launches(torch, clipped_step, 20, side)
+        nbytes = sum(((N_REPLICAS + 1) * 4 + 20) * b[1] for b in plan4["buckets"])
+        rows["clipped_step_gpt2_small"] = {"workload": "GPT-2 small, 8 fp32 accumulated replicas: average with norm "
+                                                       "side output, clip to 1.0, SGD momentum 0.9 wd 1e-4",
+                                           "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
+                                           "frac": nbytes / ms / 1e6 / peak, "launches": 5}
+        del acc, gavg, theta, buf
 
-    # SyncBN, 4 shapes
-    for C, H, W in workloads.SYNCBN_SHAPES:
-        B = workloads.SYNCBN_BATCH
-        xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, workloads.seed_for(4, r), device=dev,
-                                      dtype=torch.bfloat16) for r in range(N_REPLICAS)]
-        ys = [torch.empty_like(x) for x in xs]
-        ws = torch.empty(g.syncbn_workspace_bytes(N_REPLICAS, B, C, H, W), dtype=torch.uint8, device=dev)
-        mean = torch.empty(C, device=dev)
-        inv = torch.empty(C, device=dev)
-        # SYNCBN_CALLS back-to-back calls per graph replay (as consecutive BN layers sit in a captured
-        # step), so the figure is device time per call, not one graph launch's latency per call
-        ms = _time_launches(torch, lambda: [g.syncbn_merge_apply(xs, ys, mean, inv, ws) for _ in range(SYNCBN_CALLS)],
-                            10, side) / SYNCBN_CALLS
-        nbytes = 6 * N_REPLICAS * B * C * H * W
-        rows[f"syncbn_{C}x{H}x{W}"] = {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
-                                       "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-                                       "launches": 3, "calls_per_graph": SYNCBN_CALLS,
-                                       "note": "inputs smaller than L2" if nbytes / 3 < L2_BYTES else ""}
-        del xs, ys
+    if want("orders"):
+        # the ResNet-50 step in the other reduction orders (ring chunks, pairwise tree), same schedule
+        num_r = workloads.numels(workloads.resnet50_layout())
+        plan_r = g.ddp_plan_buckets(num_r, 4, 25 << 20)
+        reps_r = [workloads.device_normal((plan_r["total_elems"],), 0.0, 0.01, workloads.seed_for(2, r), device=dev)
+                  for r in range(N_REPLICAS)]
+        out_r = torch.empty(plan_r["total_elems"], device=dev)
+        pool_r = [torch.cuda.Stream(device=dev) for _ in range(len(plan_r["buckets"]))]
+        nbytes = sum((N_REPLICAS + 1) * 4 * b[1] for b in plan_r["buckets"])
+        for name, flag in (("ring", g.FLAG_RING_ORDER), ("tree", g.FLAG_TREE_ORDER)):
+            def ordered(flag=flag):
+                _fan_out(torch, [lambda off=off, n=n: g.ddp_bucket_allreduce_mean(
+                    [x[off:off + n] for x in reps_r], out_r[off:off + n], flags=flag)
+                    for off, n, _, _ in plan_r["buckets"]], pool_r)
+            ms = _time_launches(torch, ordered, 200, side)
+            rows[f"mean_{name}_order_resnet50"] = {
+                "workload": f"ResNet-50 step (5 x 25 MiB buckets, 8 fp32 replicas), {name}-order reduction",
+                "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+                "launches": len(plan_r["buckets"])}
+        del reps_r, out_r
 
-    # sampler
-    n, N = workloads.SAMPLER_N_ITEMS, workloads.SAMPLER_REPLICAS
-    out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
-    ms = _time_launches(torch, lambda: [g.dist_sampler_indices(n, N, -1, 0, 1 + e, True, False, out)
-                                        for e in range(SAMPLER_CALLS)], 10, side) / SAMPLER_CALLS
-    # Integer-pipe roofline: the launch's measured instruction stream at full issue -- the slowest of
-    # ALU pipe (2 / SM cycle), FMA-heavy pipe (2 / SM cycle) and issue (4 / SM cycle), 152 SMs, 2.07 GHz
-    sm_cycles = max(SAMPLER_WARP_INST["alu"] / 2, SAMPLER_WARP_INST["fmaheavy"] / 2, SAMPLER_WARP_INST["all"] / 4) / 152
-    idx_per_s = out.numel() / (ms * 1e-3)
-    peak_idx = out.numel() / (sm_cycles / 2.07e9)
-    rows["sampler_imagenet"] = {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
-                                "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
-                                "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
-                                "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
-                                "launches": 1, "calls_per_graph": SAMPLER_CALLS}
-    # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point): 1 KiB .. 1 GiB
-    # per replica in x4 steps, N in {2, 4, 8, 16}, caps {1, 25, 100} MiB; a cap that does not change the
-    # launch count is measured once; the 1 MiB split also as grouped launches (up to 1024 buckets each)
-    sweep = []
-    for size in [1 << (10 + 2 * k) for k in range(11)]:
-        numel = size // 4
-        for n in (2, 4, 8, 16):
-            reps = [workloads.device_normal((numel,), 0.0, 1.0, workloads.seed_for(5, r), device=dev)
-                    for r in range(n)]
-            outs = torch.empty(numel, device=dev)
-            nbytes = (n + 1) * size
-            l2 = "working set in L2" if nbytes < L2_BYTES else "larger than L2"
-            iters = 200 if size <= (64 << 20) else 20
-            seen = set()
-            for cap in (1 << 20, 25 << 20, 100 << 20):
-                ce = cap // 4
-                nl = -(-numel // ce)
-                if nl in seen:
-                    continue
-                seen.add(nl)
+    if want("syncbn"):
+        # SyncBN, 4 shapes
+        for C, H, W in workloads.SYNCBN_SHAPES:
+            B = workloads.SYNCBN_BATCH
+            xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, workloads.seed_for(4, r), device=dev,
+                                          dtype=torch.bfloat16) for r in range(N_REPLICAS)]
+            ys = [torch.empty_like(x) for x in xs]
+            ws = torch.empty(g.syncbn_workspace_bytes(N_REPLICAS, B, C, H, W), dtype=torch.uint8, device=dev)
+            mean = torch.empty(C, device=dev)
+            inv = torch.empty(C, device=dev)
+            # SYNCBN_CALLS back-to-back calls per graph replay (as consecutive BN layers sit in a captured
+            # step), so the figure is device time per call, not one graph launch's latency per call
+            ms = _time_launches(torch, lambda: [g.syncbn_merge_apply(xs, ys, mean, inv, ws) for _ in range(SYNCBN_CALLS)],
+                                10, side) / SYNCBN_CALLS
+            nbytes = 6 * N_REPLICAS * B * C * H * W
+            rows[f"syncbn_{C}x{H}x{W}"] = {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
+                                           "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
+                                           "launches": 3, "calls_per_graph": SYNCBN_CALLS,
+                                           "note": "inputs smaller than L2" if nbytes / 3 < L2_BYTES else ""}
+            del xs, ys
 
-                def flat_step(reps=reps, outs=outs, ce=ce, numel=numel):
-                    for s0 in range(0, numel, ce):
-                        e = min(numel, s0 + ce)
-                        g.ddp_bucket_allreduce_mean([x[s0:e] for x in reps], outs[s0:e])
-                ms = _time_launches(torch, flat_step, iters, side)
-                sweep.append({"bytes_per_replica": size, "replicas": n,
-                              "cap_mib": cap >> 20 if nl > 1 else "any (one launch)",
-                              "launches": nl, "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
-                              "frac": nbytes / ms / 1e6 / peak, "l2": l2})
-                if nl > 1 and cap == (1 << 20):
-                    bl = [(s0, min(ce, numel - s0)) for s0 in range(0, numel, ce)]
+    if want("sampler"):
+        # sampler
+        n, N = workloads.SAMPLER_N_ITEMS, workloads.SAMPLER_REPLICAS
+        out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
+        ms = _time_launches(torch, lambda: [g.dist_sampler_indices(n, N, -1, 0, 1 + e, True, False, out)
+                                            for e in range(SAMPLER_CALLS)], 10, side) / SAMPLER_CALLS
+        # Integer-pipe roofline: the launch's measured instruction stream at full issue -- the slowest of
+        # ALU pipe (2 / SM cycle), FMA-heavy pipe (2 / SM cycle) and issue (4 / SM cycle), 152 SMs, 2.07 GHz
+        sm_cycles = max(SAMPLER_WARP_INST["alu"] / 2, SAMPLER_WARP_INST["fmaheavy"] / 2, SAMPLER_WARP_INST["all"] / 4) / 152
+        idx_per_s = out.numel() / (ms * 1e-3)
+        peak_idx = out.numel() / (sm_cycles / 2.07e9)
+        rows["sampler_imagenet"] = {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
+                                    "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
+                                    "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
+                                    "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
+                                    "launches": 1, "calls_per_graph": SAMPLER_CALLS}
+    if want("sweep"):
+        # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point): 1 KiB .. 1 GiB
+        # per replica in x4 steps, N in {2, 4, 8, 16}, caps {1, 25, 100} MiB; a cap that does not change the
+        # launch count is measured once; the 1 MiB split also as grouped launches (up to 1024 buckets each)
+        sweep = []
+        for size in [1 << (10 + 2 * k) for k in range(11)]:
+            numel = size // 4
+            for n in (2, 4, 8, 16):
+                reps = [workloads.device_normal((numel,), 0.0, 1.0, workloads.seed_for(5, r), device=dev)
+                        for r in range(n)]
+                outs = torch.empty(numel, device=dev)
+                nbytes = (n + 1) * size
+                l2 = "working set in L2" if nbytes < L2_BYTES else "larger than L2"
+                iters = 200 if size <= (64 << 20) else 20
+                seen = set()
+                for cap in (1 << 20, 25 << 20, 100 << 20):
+                    ce = cap // 4
+                    nl = -(-numel // ce)
+                    if nl in seen:
+                        continue
+                    seen.add(nl)
 
-                    def grouped(reps=reps, outs=outs, bl=bl):
-                        for i in range(0, len(bl), 1024):
-                            g.ddp_bucket_allreduce_mean_multi(reps, bl[i:i + 1024], outs)
-                    ms = _time_launches(torch, grouped, iters, side)
-                    sweep.append({"bytes_per_replica": size, "replicas": n, "cap_mib": 1,
-                                  "launches": -(-len(bl) // 1024), "grouped": True, "us": ms * 1e3,
-                                  "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "l2": l2})
-            del reps, outs
-    rows["sweep_flat_fp32"] = sweep
+                    def flat_step(reps=reps, outs=outs, ce=ce, numel=numel):
+                        for s0 in range(0, numel, ce):
+                            e = min(numel, s0 + ce)
+                            g.ddp_bucket_allreduce_mean([x[s0:e] for x in reps], outs[s0:e])
+                    ms = _time_launches(torch, flat_step, iters, side)
+                    sweep.append({"bytes_per_replica": size, "replicas": n,
+                                  "cap_mib": cap >> 20 if nl > 1 else "any (one launch)",
+                                  "launches": nl, "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
+                                  "frac": nbytes / ms / 1e6 / peak, "l2": l2})
+                    if nl > 1 and cap == (1 << 20):
+                        bl = [(s0, min(ce, numel - s0)) for s0 in range(0, numel, ce)]
+
+                        def grouped(reps=reps, outs=outs, bl=bl):
+                            for i in range(0, len(bl), 1024):
+                                g.ddp_bucket_allreduce_mean_multi(reps, bl[i:i + 1024], outs)
+                        ms = _time_launches(torch, grouped, iters, side)
+                        sweep.append({"bytes_per_replica": size, "replicas": n, "cap_mib": 1,
+                                      "launches": -(-len(bl) // 1024), "grouped": True, "us": ms * 1e3,
+                                      "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "l2": l2})
+                del reps, outs
+        rows["sweep_flat_fp32"] = sweep
     rows["_peak"] = {"hbm_gbs": peak, "source": peak_kind}
     return rows
 
