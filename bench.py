@@ -62,8 +62,8 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-rows", action="store_true", help="skip the SGD / SyncBN / sampler rows")
     p.add_argument("--rows", default=None,
-                   help="comma-separated subset of the side-row groups to run: gpt2 (SGD, SGD with the bf16 copy, "
-                        "bf16 average), accum (accumulation, clipped step), orders (ring and tree order), syncbn, "
+                   help="comma-separated subset of the side-row groups to run: linear (the Linear(128,10) step's "
+                        "latency), gpt2 (SGD, SGD with the bf16 copy, bf16 average), accum (accumulation, clipped step), orders (ring and tree order), syncbn, "
                         "sampler, sweep; default all")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
@@ -586,6 +586,22 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
 
     layout, first = workloads.gpt2_small_layout()      # GPT-2 small parameter list (gpt2 and accum rows)
     num = workloads.numels(layout)
+
+    if want("linear"):
+        # Linear(128,10): 4 fp32 replicas of 1,290 gradient elements, average + SGD lr 0.1 (no momentum) in one
+        # launch; 31 KB per step, so the figure is the call's latency (20 calls per graph replay)
+        numel_l = sum(workloads.numels(workloads.linear_128_10_layout()))   # 1,290
+        reps_l = [workloads.device_normal((numel_l,), 0.0, 1.0, workloads.seed_for(1, r), device=dev) for r in range(4)]
+        theta_l = workloads.device_normal((numel_l,), 0.0, 0.1, workloads.seed_for(1, 99), device=dev)
+        ms = _time_launches(torch, lambda: [g.ddp_bucket_allreduce_sgd(reps_l, theta_l, None, 0.1, 0.0, 0.0)
+                                            for _ in range(20)], 10, side) / 20
+        nbytes = (4 * 4 + 8) * numel_l
+        rows["sgd_linear_128_10"] = {"workload": "Linear(128,10), 4 fp32 replicas (1,290 elements), average + SGD "
+                                                 "lr 0.1 in one launch", "ms": ms, "us": ms * 1e3, "bytes": nbytes,
+                                     "GBps": nbytes / ms / 1e6, "frac": None, "launches": 1,
+                                     "note": "latency-bound (31 KB per call): the figure is µs per call",
+                                     "calls_per_graph": 20}
+        del reps_l, theta_l
 
     if want("gpt2"):
         # fused SGD, GPT-2 small DEEP/FIRST, bf16 grads, momentum 0.9, wd 1e-4
