@@ -1,5 +1,5 @@
 // Strict SyncBatchNorm forward across N replicas on one GPU: per-channel
-// statistics of the global batch, merged in fp64, then the normalisation.
+// statistics of the global batch, merged in float-float, then the normalisation.
 //
 // Tech-Renaissance "(24) NCCL通信与分布式数据并行" §十二: strict SyncBatchNorm
 // all-reduces every rank's sum and sum of squares before BN finalize/apply.
@@ -34,13 +34,12 @@
 //      reductions) and stores one fp32 (sum, sum of squares) partial per
 //      channel and slice.
 //   2. merge  — one warp per channel sums the S partials in a fixed order in
-//      float-float (fp32 pairs), then one thread per channel finalises: in
-//      fp64, with m' = Σd/M, mean = K_c + m' and var = Σd²/M − m'² (the same
-//      S/M and Q/M − mean² up to rounding); in fp32, invstd =
-//      1/sqrt(var + eps) with IEEE-rounded sqrt and divide.  With the mean
-//      split into an fp32 pair m_hi + m_lo and scale = invstd·γ, it stores
-//      per channel (m_hi, scale, shift), shift = β − m_lo·scale formed in
-//      fp64 and rounded once.
+//      float-float (fp32 pairs), then its lane 0 finalises in float-float:
+//      m' = Σd/M, mean = K_c + m' and var = Σd²/M − m'² (the same S/M and
+//      Q/M − mean² up to rounding); in fp32, invstd = 1/sqrt(var + eps) with
+//      IEEE-rounded sqrt and divide.  With the mean as an fp32 pair
+//      m_hi + m_lo and scale = invstd·γ, it stores per channel (m_hi, scale,
+//      shift), shift = β − m_lo·scale rounded once.
 //   3. apply  — y = (x − m_hi)·scale + shift over every replica, 16-byte
 //      vectors in and out, the channel computed once per 8-element vector,
 //      element pairs in packed f32x2 arithmetic.  x − m_hi is exact when x
@@ -89,7 +88,8 @@ struct BnParams {
     int32_t tc_log2;    // bulk kernel: log2 of the lanes per channel (32/G for G < 32, else 0)
     uint64_t buf_fl;    // bulk kernel: replica bytes rounded down to 16 (copies stop there)
     float eps;
-    double inv_count;   // 1 / (n * batch * H * W)
+    float inv_hi, inv_lo;  // 1 / (n * batch * H * W) as a float pair
+    int32_t tree_top;      // merge: first shuffle offset (lanes >= min(S, 32) hold no sums)
 };
 
 template <bool BF16>
@@ -597,10 +597,25 @@ __global__ void __launch_bounds__(kThreads) bn_stats_element_kernel(const __grid
         a.partial[static_cast<int64_t>(c) * a.S + s] = make_float2(__fadd_rn(fs.hi, fs.lo), __fadd_rn(fq.hi, fq.lo));
 }
 
+// Float-float product: Dekker's product with the exact low part of
+// a.hi·b.hi from a fused multiply-add, plus the cross terms.
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+    const float p = __fmul_rn(a.hi, b.hi);
+    const float e = fmaf(a.hi, b.hi, -p);
+    const float t = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
+    const float hi = __fadd_rn(p, t);
+    return FF{hi, __fsub_rn(t, __fsub_rn(hi, p))};
+}
+
 // CTA of 32 warps = 32 channels.  Warp w adds channel (32·blockIdx + w)'s S
-// partials in float-float (lane l takes slices l, l+32, ..., then a fixed
-// shuffle tree); warp 0 then finalises the 32 channels in fp64, one channel
-// per lane, so each fp64 instruction serves 32 channels.
+// partials in float-float (lane l takes slices l, l + 32, ..., then a fixed
+// shuffle tree only as deep as the lanes that hold sums); warp 0 then
+// finalises the 32 channels, one per lane, in float-float on the fp32 pipe
+// (GB300's fp64 pipe is narrow: a dozen dependent fp64 operations cost more
+// than the rest of the merge): m' = Σd/M, mean = K_c + m',
+// var = Σd²/M − m'², invstd = 1/sqrt(var + eps) in fp32 with IEEE sqrt and
+// divide, and the coefficients (m_hi, scale, shift) with
+// shift = β − m_lo·scale rounded once.
 constexpr int kMergeThreads = 1024;
 
 template <bool BF16>
@@ -632,8 +647,7 @@ __global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_co
             Q = ff_add(Q, FF{v.y, 0.0f});
         }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = a.tree_top; o > 0; o >>= 1) {    // lanes >= min(S, 32) hold zeros
         S = ff_add(S, ff_shfl_down(S, o));
         Q = ff_add(Q, ff_shfl_down(Q, o));
     }
@@ -643,23 +657,19 @@ __global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_co
     }
     __syncthreads();
     if (w != 0 || cc >= a.C) return;
-    // fp64: the sums, the mean and the variance; fp32: 1/sqrt(var + eps) (IEEE sqrt and divide,
-    // relative error ~2^-23, far inside what the normalisation needs) and the scale
-    const double Sd = static_cast<double>(sums[0][lane].hi) + static_cast<double>(sums[0][lane].lo);
-    const double Qd = static_cast<double>(sums[1][lane].hi) + static_cast<double>(sums[1][lane].lo);
-    const double ms = Sd * a.inv_count;                    // mean of the shifted values
-    const double mean = static_cast<double>(Kc) + ms;
-    const double var = Qd * a.inv_count - ms * ms;
-    const float invstd = 1.0f / sqrtf(static_cast<float>(var + static_cast<double>(a.eps)));
-    const float m_hi = static_cast<float>(mean);
-    a.mean_out[cc] = m_hi;
+    const FF inv{a.inv_hi, a.inv_lo};            // 1/M as a float pair
+    const FF ms = ff_mul(sums[0][lane], inv);    // mean of the shifted values
+    const FF mean = ff_add(FF{Kc, 0.0f}, ms);
+    const FF ms2 = ff_mul(ms, ms);
+    const FF var = ff_add(ff_mul(sums[1][lane], inv), FF{-ms2.hi, -ms2.lo});
+    const FF ve = ff_add(var, FF{a.eps, 0.0f});
+    const float invstd = 1.0f / sqrtf(ve.hi);
+    a.mean_out[cc] = mean.hi;
     a.invstd_out[cc] = invstd;
     // y = (x − mean)·scale + β = (x − m_hi)·scale + (β − m_lo·scale): the low part of the mean
-    // goes into the shift (fp64, rounded once), so x − m_hi is the apply's only subtraction
+    // goes into the shift (one rounding), so x − m_hi is the apply's only subtraction
     const float scale = invstd * gc;
-    const double m_lo = mean - static_cast<double>(m_hi);
-    a.coef[cc] = make_float4(m_hi, scale, static_cast<float>(static_cast<double>(bc) - m_lo * static_cast<double>(scale)),
-                             0.0f);
+    a.coef[cc] = make_float4(mean.hi, scale, fmaf(-mean.lo, scale, bc), 0.0f);
 }
 
 // (x − m_hi)·scale + shift with k = (m_hi, scale, shift, unused)
@@ -1040,7 +1050,13 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     p.tc_log2 = 0;
     while (sp.G < 32 && (sp.G << p.tc_log2) < 32) ++p.tc_log2;
     p.eps = eps;
-    p.inv_count = 1.0 / (static_cast<double>(n_replicas) * batch * p.HW);
+    const double inv_count = 1.0 / (static_cast<double>(n_replicas) * batch * p.HW);
+    p.inv_hi = static_cast<float>(inv_count);
+    p.inv_lo = static_cast<float>(inv_count - static_cast<double>(p.inv_hi));
+    const int lanes = sp.S < 32 ? sp.S : 32;      // lanes of a merge warp that hold sums
+    int top = 1;
+    while (top < lanes) top *= 2;
+    p.tree_top = top / 2;                           // 0 for a single slice
     char* ws = static_cast<char*>(workspace);
     p.partial = reinterpret_cast<float2*>(ws);
     ws += align_up(static_cast<size_t>(C) * p.S * sizeof(float2), 16);

@@ -380,8 +380,8 @@ size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int3
  * not cancel when |mean| >> std); threads accumulate a few hundred
  * elements in fp32, each CTA combines its threads in float-float (pairs of
  * fp32) and stores one fp32 partial per channel and slice of the samples,
- * and a merge kernel sums the partials in float-float and finalises in
- * fp64; the apply runs in fp32.
+ * and a merge kernel sums the partials and finalises in float-float; the
+ * apply runs in fp32.
  *
  *   x            host array of n_replicas device pointers, each
  *                [batch, C, H, W] NCHW contiguous, in_dtype elements

@@ -1,7 +1,7 @@
 """GPU parity: syncbn_merge_apply against the fp64 oracle.
 
 Tolerances (the computation is not bit-reproducible by design: fp32 partial
-sums, fp64 merge, fp32 apply):
+sums, float-float merge, fp32 apply):
   mean, invstd       |gpu − oracle| <= 1e-5 · |oracle| (+1e-7 absolute for a mean near 0)
   y (fp32 output)    |gpu − oracle| <= 1e-5 · |oracle| + 1e-6
   y (bf16 output)    within one bf16 ulp of the oracle's fp64 value rounded to
