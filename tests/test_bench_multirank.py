@@ -70,3 +70,27 @@ def test_torchrun_reference_arm_two_ranks_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["unit"] == "GB/s"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_rows_option_names_every_group():
+    """`--rows` selects side-row groups by name: the names its help text
+    lists are exactly the groups bench_rows guards, so no group can be
+    skipped by a misspelt name in either place."""
+    import inspect
+    import re
+    sys.path.insert(0, ROOT)
+    import bench
+    guarded = set(re.findall(r'if want\("(\w+)"\)', inspect.getsource(bench.bench_rows)))
+    src = inspect.getsource(bench.parse_args)
+    help_text = "".join(re.findall(r'"([^"]*)"', src[src.index('"--rows"'):src.index("return p.parse_args")]))
+    listed = set(re.findall(r"\b([a-z0-9]+) \(", help_text)) | set(re.findall(r"\b(syncbn|sampler|sweep)\b", help_text))
+    assert guarded == {"linear", "gpt2", "accum", "orders", "syncbn", "sampler", "sweep"}, guarded
+    assert guarded <= listed, (guarded, listed)
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py", "--rows", "syncbn,sampler"]
+        assert bench.parse_args().rows == "syncbn,sampler"
+        sys.argv = ["bench.py"]
+        assert bench.parse_args().rows is None
+    finally:
+        sys.argv = old
