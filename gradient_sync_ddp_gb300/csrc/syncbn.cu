@@ -150,6 +150,16 @@ __device__ __forceinline__ void slice_bounds(const BnParams& a, int s, int& p0, 
     }
 }
 
+// Start of the statistics kernels: wait for the previous grid in the stream
+// (full completion and memory flush) before letting this call's merge and
+// apply launch.  The apply reads its first vectors of x before its own wait,
+// which is safe only once every kernel issued before this call (one of them
+// may have written x, e.g. the previous layer's apply) has completed.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Group kernel, grid (ceil(C/G), S).
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_constant__ BnParams a) {
@@ -165,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
     slice_bounds(a, s, p0, p1);
     const uint64_t run_bytes = static_cast<uint64_t>(Gc) * a.HW * ESZ;
     const uint32_t vslot = static_cast<uint32_t>(a.slot_bytes / 16);
-    pdl_enter();
+    pdl_wait_then_release();
     const float K = active ? load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + cl) * a.HW) : 0.0f;
 
     float acc_s = 0.0f, acc_q = 0.0f;
@@ -364,7 +374,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     const uint32_t e_hi = (static_cast<uint32_t>(HW) * (part + 1)) >> a.tc_log2;
     int cl[CPL];
     float K[CPL], acc_s[CPL], acc_q[CPL];
-    pdl_enter();
+    pdl_wait_then_release();
 #pragma unroll
     for (int m = 0; m < CPL; ++m) {
         cl[m] = a.G >= 32 ? lane + 32 * m : lane >> a.tc_log2;
@@ -509,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 5) bn_stats_plane_kernel(const __gri
     const uint32_t units = static_cast<uint32_t>(a.HW / W);                     // vectors per plane
     const uint32_t cpp = (units + kChunkVecs - 1) / kChunkVecs;                  // chunks per plane
     const uint32_t total = static_cast<uint32_t>(p1 - p0) * cpp;
-    pdl_enter();
+    pdl_wait_then_release();
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
     // one (Σd, Σd²) pair per element position of the vector: each sums one element per vector (as
     // many terms as a per-vector total would), at one add and one fused multiply-add per element,
@@ -578,7 +588,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_element_kernel(const __grid
     const int c = blockIdx.x, s = blockIdx.y;
     int p0, p1;
     slice_bounds(a, s, p0, p1);
-    pdl_enter();
+    pdl_wait_then_release();
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);
     float acc_s = 0.0f, acc_q = 0.0f;
     for (int pl = p0; pl < p1; ++pl) {
@@ -700,10 +710,9 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
     const uint32_t nvec = E / 8;
     const uint32_t stride = gridDim.x * kThreads;
     const uint32_t gtid = blockIdx.x * kThreads + threadIdx.x;
-    pdl_enter();
-    for (uint32_t v0 = gtid; v0 < nvec; v0 += 4 * stride) {
-        // issue the loads of 4 vectors before any arithmetic
-        uint4 raw[4][2];
+    // the loads of 4 vectors, issued before any arithmetic
+    uint4 raw[4][2];
+    auto load4 = [&](uint32_t v0) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const uint32_t v = v0 + u * stride;
@@ -712,6 +721,14 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
                 if constexpr (!BF16_IN) raw[u][1] = ld16<NC>(x + static_cast<int64_t>(v) * 8 * ISZ + 16);
             }
         }
+    };
+    // the first iteration's x before the wait, overlapping the merge: x depends on no kernel of
+    // this call, and the statistics kernel let this one launch only after every earlier kernel
+    // in the stream had completed; the coefficients are read after the wait
+    if (gtid < nvec) load4(gtid);
+    pdl_enter();
+    for (uint32_t v0 = gtid; v0 < nvec; v0 += 4 * stride) {
+        if (v0 != gtid) load4(v0);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const uint32_t v = v0 + u * stride;

@@ -165,3 +165,39 @@ def test_large_mean_small_std(g):
         # x − mean is exact in fp32 near 1000 only to ~6e-5 absolute (fp32 spacing of the input
         # itself): y inherits that times invstd ≈ 10, so compare with 1e-3 absolute here
         assert np.all(np.abs(got - y_w[r]) <= 1e-5 * np.abs(y_w[r]) + 1e-3)
+
+
+@pytest.mark.parametrize("shape,in_place", [((8, 32, 128, 28, 28), False), ((8, 32, 256, 14, 14), False),
+                                            ((8, 32, 128, 28, 28), True)])
+def test_chained_layers_equal_separate_calls(g, shape, in_place):
+    """Three SyncBN calls back to back on one stream, each reading the
+    previous call's output: a call's apply reads its first vectors of x
+    before waiting for its merge, so it must not start before the previous
+    call's apply has written that x.  The chained result equals, bit for
+    bit, the same three calls each followed by a device synchronisation
+    (the kernels' reduction orders are fixed, so equal inputs give equal
+    bits).  Aligned 28x28 planes (plane statistics) and unaligned 14x14
+    planes (bulk-staged statistics), out of place and in place."""
+    n, B, C, H, W = shape
+    xs = [dev_bf16(x) for x in workloads.syncbn_input(4, n, B, C, H, W)]
+    ws = torch.empty(g.syncbn_workspace_bytes(n, B, C, H, W), dtype=torch.uint8, device="cuda")
+    mean, invstd = torch.empty(C, device="cuda"), torch.empty(C, device="cuda")
+
+    def three_layers(sync_each):
+        cur = [x.clone() for x in xs]
+        for _ in range(3):
+            nxt = cur if in_place else [torch.empty_like(x) for x in cur]
+            g.syncbn_merge_apply(cur, nxt, mean, invstd, ws)
+            if sync_each:
+                sync()
+            cur = nxt
+        sync()
+        return [c.clone() for c in cur], mean.clone(), invstd.clone()
+
+    sep, m_sep, s_sep = three_layers(True)
+    for _ in range(3):
+        got, m_got, s_got = three_layers(False)
+        assert torch.equal(m_got.view(torch.int32), m_sep.view(torch.int32))
+        assert torch.equal(s_got.view(torch.int32), s_sep.view(torch.int32))
+        for r in range(n):
+            assert torch.equal(got[r].view(torch.int16), sep[r].view(torch.int16)), f"replica {r}"
