@@ -63,7 +63,7 @@ constexpr int64_t kMaxPartials = 65536;  // C*S bound: fp32 partials stay <= 512
 constexpr int kRunElems = 2048;          // channels per group: G*H*W <= this (G >= 1)
 constexpr int kStageBytes = 32768;       // shared staging buffer per CTA (staged group kernel)
 constexpr int kPlaneVecsPerThread = 24;  // plane statistics: slices sized for this many vectors per thread
-constexpr int kApplyWaves = 8;           // apply grid: at most this many waves of resident CTAs
+constexpr int kApplyWaves = 16;          // apply grid: at most this many waves of resident CTAs
 constexpr int kApplyVecs = 8;            // apply grid: at least this many 16-byte vectors per thread
 
 struct BnParams {
