@@ -201,3 +201,31 @@ def test_chained_layers_equal_separate_calls(g, shape, in_place):
         assert torch.equal(s_got.view(torch.int32), s_sep.view(torch.int32))
         for r in range(n):
             assert torch.equal(got[r].view(torch.int16), sep[r].view(torch.int16)), f"replica {r}"
+
+
+@pytest.mark.parametrize("shape", [(4, 2, 6, 8, 8), (4, 2, 6, 7, 7)])
+def test_non_finite_channel_stays_in_its_channel(g, shape):
+    """A NaN in channel 1 and an infinity in channel 4 of one replica: those
+    channels' statistics are not finite (the oracle's are not either), and
+    every other channel's mean, invstd and output match the oracle, so a
+    non-finite activation reaches no other channel (aligned 8x8 and
+    unaligned 7x7 planes)."""
+    n, B, C, H, W = shape
+    xs = workloads.syncbn_input(4, n, B, C, H, W)
+    xs[2][1, 1, 3, 2] = 0x7FC0          # NaN
+    xs[1][0, 4, 5, 5] = 0x7F80          # +inf
+    xs_dev = [dev_bf16(x) for x in xs]
+    ys = [torch.empty((B, C, H, W), device="cuda") for _ in range(n)]
+    mean, invstd = _run(g, xs_dev, ys, C)
+    with np.errstate(invalid="ignore"):
+        m_w, s_w, y_w = oracle.syncbn(xs, 1e-5)
+    m, s = mean.cpu().numpy().astype(np.float64), invstd.cpu().numpy().astype(np.float64)
+    bad = [1, 4]
+    for c in bad:
+        assert not (np.isfinite(m_w[c]) and np.isfinite(s_w[c]))
+        assert not (np.isfinite(m[c]) and np.isfinite(s[c])), (c, m[c], s[c])
+    good = [c for c in range(C) if c not in bad]
+    assert np.all(np.abs(m[good] - m_w[good]) <= 1e-5 * np.abs(m_w[good]) + 1e-7)
+    assert np.all(np.abs(s[good] - s_w[good]) <= 1e-5 * np.abs(s_w[good]))
+    for r in range(n):
+        _check_y(ys[r][:, good], np.asarray(y_w[r])[:, good], f"{shape} y[{r}] finite channels")
