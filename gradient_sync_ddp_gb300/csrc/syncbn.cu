@@ -63,7 +63,7 @@ constexpr int64_t kMaxPartials = 65536;  // C*S bound: fp32 partials stay <= 512
 constexpr int kRunElems = 2048;          // channels per group: G*H*W <= this (G >= 1)
 constexpr int kStageBytes = 32768;       // shared staging buffer per CTA (staged group kernel)
 constexpr int kPlaneVecsPerThread = 24;  // plane statistics: slices sized for this many vectors per thread
-constexpr int kApplyWaves = 16;          // apply grid: at most this many waves of resident CTAs
+constexpr int kApplyWaves = 16;          // apply grid: at most this many waves of 8 CTAs per SM
 constexpr int kApplyVecs = 8;            // apply grid: at least this many 16-byte vectors per thread
 
 struct BnParams {
@@ -1116,7 +1116,9 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     if ((st = current_device_info(&d)) != DDP_OK) return st;
     const int64_t nvec = static_cast<int64_t>(E / 8);
     // at least kApplyVecs vectors per thread (two passes of its 4-vector unroll), and at most
-    // kApplyWaves waves of resident CTAs: several waves stream faster than one grid-stride wave
+    // kApplyWaves waves counted at the SM's thread limit (8 CTAs of 256 threads; registers
+    // allow 5-6, so the grid runs more real waves): several waves stream faster than one
+    // grid-stride wave, and grids rounded to whole real waves measured slower
     int64_t gx = (nvec + static_cast<int64_t>(kThreads) * kApplyVecs - 1) / (static_cast<int64_t>(kThreads) * kApplyVecs);
     const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
     int64_t cap = (kApplyWaves * resident + n_replicas - 1) / n_replicas;
