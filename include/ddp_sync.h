@@ -394,7 +394,10 @@ size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int3
  *                match (in place), no other overlap
  *   mean_out, invstd_out   device float[C] each
  *   workspace    device buffer of >= syncbn_workspace_bytes(...) bytes,
- *                16-byte aligned, contents ignored on entry
+ *                16-byte aligned, contents ignored on entry; calls whose
+ *                kernels may overlap on the GPU (different streams without
+ *                ordering) need different workspaces, or they race on the
+ *                partial sums
  */
 int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtype,
                        int32_t batch, int32_t C, int32_t H, int32_t W, float eps,
