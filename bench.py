@@ -65,6 +65,7 @@ def parse_args():
                    help="comma-separated subset of the side-row groups to run: linear (the Linear(128,10) step's "
                         "latency), gpt2 (SGD, SGD with the bf16 copy, bf16 average), accum (accumulation, clipped step), orders (ring and tree order), syncbn, "
                         "sampler, sweep; default all")
+    p.add_argument("--rows-out", default=None, help="also append every side-row line to this file")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work budget of the oracle baseline")
     return p.parse_args()
@@ -377,7 +378,6 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
 
     step_bytes = algorithmic_bytes(plan)
-    bucket_bytes = [(N_REPLICAS + 1) * 4 * b[1] for b in buckets]
     nb = len(buckets)
     K, W = args.steps, args.warmup
 
@@ -409,48 +409,65 @@ def run_ours(args, world, rank, local):
     elapsed_ms = dist_max(local_ms, world, dev)
     value = weak_scaling_rate(world, step_bytes, K, elapsed_ms)
 
-    # The timed region runs nothing but the averaging kernel (K x 5 launches
-    # back to back), so its average launch duration is the region time over
-    # the launches, on this rank's stream.
-    avg_launch_ms = local_ms / (K * nb)
+    # The dominant kernel's own launch duration.  Inside the step the 5 launches overlap on their
+    # streams, so the step time over 5 is not one launch's duration.  Here the same 5 launches run
+    # one after another on the side stream (one graph, K replays between events on that stream):
+    # each launch then has the GPU to itself, and the region time over the K x 5 launches is the
+    # kernel's average launch duration.
+    serial_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(serial_graph, stream=side):
+        for b in range(nb):
+            launch(b)
+    with torch.cuda.stream(side):
+        for _ in range(max(W, 3)):
+            serial_graph.replay()
+    torch.cuda.synchronize()
+    k_start, k_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        k_start.record()
+        for _ in range(K):
+            serial_graph.replay()
+        k_end.record()
+    torch.cuda.synchronize()
+    avg_launch_ms = k_start.elapsed_time(k_end) / (K * nb)
     achieved = (step_bytes / nb) / (avg_launch_ms * 1e-3) / 1e9
     peak, peak_kind = load_peak()
     traffic, traffic_note = profile_traffic(kernel_source_hash(), step_bytes / nb / ((N_REPLICAS + 1) * 4))
 
-    # diagnostic (not the headline): each bucket's launch timed on its own, eagerly
-    per_bucket_us = []
-    with torch.cuda.stream(side):
-        for b in range(nb):
-            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ea.record()
-            for _ in range(20):
-                launch(b)
-            eb.record()
-            per_bucket_us.append((ea, eb))
-    torch.cuda.synchronize()
-    per_bucket_us = [ea.elapsed_time(eb) / 20 * 1e3 for ea, eb in per_bucket_us]
-
     # End to end through the public API, host buffers in and out, two ways:
-    #  "copy":      copy-engine copies of the replicas from pinned host memory into HBM, the 5 bucket calls on
-    #               device buffers, the result copied back to pinned host memory;
-    #  "zero-copy": the same 5 bucket calls given the pinned host buffers themselves — the kernels read the
+    #  "copy":      every step copies the replicas from pinned host memory into HBM bucket by bucket on one
+    #               copy stream, each bucket's average starts once its slices have arrived, and its result
+    #               goes back to pinned host memory on a third stream (the copy of bucket b's result overlaps
+    #               the inbound copies of the later buckets);
+    #  "zero-copy": the same 5 bucket calls given the pinned host buffers themselves: the kernels read the
     #               replicas over NVLink-C2C (coherent host memory) and write the average to host memory.
     host_reps = [torch.empty(total, dtype=torch.float32, pin_memory=True) for _ in range(N_REPLICAS)]
     for h, d in zip(host_reps, reps):
         h.copy_(d)
     host_out = torch.empty(total, dtype=torch.float32, pin_memory=True)
     torch.cuda.synchronize()
+    h2d_stream, k_stream, d2h_stream = (torch.cuda.Stream(device=dev) for _ in range(3))
 
     def launch_host(b):
         off, n = buckets[b][0], buckets[b][1]
         g.ddp_bucket_allreduce_mean([x[off:off + n] for x in host_reps], host_out[off:off + n])
 
     def e2e_copy_step():
-        for h, d in zip(host_reps, reps):
-            d.copy_(h, non_blocking=True)
+        cur = torch.cuda.current_stream()
+        for st in (h2d_stream, k_stream, d2h_stream):
+            st.wait_stream(cur)
         for b in range(nb):
-            launch(b)
-        host_out.copy_(out, non_blocking=True)
+            off, n = buckets[b][0], buckets[b][1]
+            with torch.cuda.stream(h2d_stream):
+                for h, d in zip(host_reps, reps):
+                    d[off:off + n].copy_(h[off:off + n], non_blocking=True)
+            k_stream.wait_stream(h2d_stream)
+            launch(b, k_stream)
+            d2h_stream.wait_stream(k_stream)
+            with torch.cuda.stream(d2h_stream):
+                host_out[off:off + n].copy_(out[off:off + n], non_blocking=True)
+        for st in (h2d_stream, k_stream, d2h_stream):
+            cur.wait_stream(st)
 
     def e2e_zero_copy_step():
         for b in range(nb):
@@ -472,6 +489,7 @@ def run_ours(args, world, rank, local):
         return weak_scaling_rate(world, step_bytes, args.e2e_steps, dist_max(e0.elapsed_time(e1), world, dev))
 
     e2e_copy = time_e2e(e2e_copy_step)
+    copy_check = bool(torch.equal(host_out, out.cpu()))
     e2e_zero = time_e2e(e2e_zero_copy_step)
 
     # the host link on its own: copy-engine H2D of the replicas, for the bound the e2e figures sit under
@@ -484,53 +502,101 @@ def run_ours(args, world, rank, local):
         l1.record()
     torch.cuda.synchronize()
     h2d_gbs = 3 * N_REPLICAS * total * 4 / (l0.elapsed_time(l1) * 1e-3) / 1e9
-    zero_read_gbs = e2e_zero * N_REPLICAS / (N_REPLICAS + 1)     # the host bytes the zero-copy kernels read
-    host_check = bool(torch.equal(host_out, out.cpu()))      # both modes computed the same average
-    e2e_value, e2e_mode = (e2e_zero, "zero-copy") if e2e_zero >= e2e_copy else (e2e_copy, "copy")
+    host_check = copy_check and bool(torch.equal(host_out, out.cpu()))   # both modes computed the same average
 
-    rows = None
+    if rank == 0:
+        # diagnostic row (not the headline): each bucket's launch timed on its own, eagerly
+        per_bucket = []
+        with torch.cuda.stream(side):
+            for b in range(nb):
+                ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ea.record()
+                for _ in range(20):
+                    launch(b)
+                eb.record()
+                per_bucket.append((ea, eb))
+        torch.cuda.synchronize()
+        emit_row("headline_buckets", {
+            "workload": "ResNet-50 step, each bucket's launch timed alone (20 eager launches each)",
+            "bytes": [(N_REPLICAS + 1) * 4 * b[1] for b in buckets],
+            "us": [ea.elapsed_time(eb) / 20 * 1e3 for ea, eb in per_bucket]}, args.rows_out)
+
     if rank == 0 and world == 1 and not args.no_rows:
         del host_reps, host_out
         only = None if args.rows is None else {r.strip() for r in args.rows.split(",") if r.strip()}
-        rows = bench_rows(g, torch, dev, peak, peak_kind, only)
+        bench_rows(g, torch, dev, peak, peak_kind, only, args.rows_out)
 
     if rank == 0:
         cpu = None if args.no_cpu_baseline or world > 1 else cpu_oracle_rate(plan, args.cpu_seconds)
         clocks = summarize_clocks(clock_rows, t_host0, t_host1)
-        line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
-            "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic: seeded N(0, 0.01) fp32 replica gradients drawn on the device",
-            "config": workload_config(plan, num),
-            "hbm_fraction": value / world / peak,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{peak_kind} (HBM copy bandwidth)",
-                         "kernel": "mean_kernel (ddp_bucket_allreduce_mean, fp32, rank order, N=8)",
-                         "algorithmic_bytes_per_launch": step_bytes / nb,
-                         "avg_launch_us": avg_launch_ms * 1e3,
-                         "per_bucket_bytes": bucket_bytes,
-                         "per_bucket_us_eager_diagnostic": per_bucket_us,
-                         **({"traffic_note": traffic_note} if traffic_note else {})},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": N_REPLICAS * total * 4,
-                    "d2h_bytes_per_step": total * 4, "steps": args.e2e_steps, "mode": e2e_mode,
-                    "copy_mode_value": e2e_copy, "zero_copy_mode_value": e2e_zero,
-                    "modes_agree_bitwise": host_check,
-                    "host_link": {"h2d_copy_GBps": h2d_gbs, "zero_copy_host_read_GBps": zero_read_gbs,
-                                  "note": "e2e is bound by the host link: the zero-copy kernels read host "
-                                          "memory at the rate copy-engine H2D copies reach"}},
-            "gpu_launches": K * nb,
-            "schedule": {"graph": "one CUDA graph per step", "bucket_streams": len(bucket_streams),
-                         "note": "each bucket launch on its own stream: the buckets are disjoint, so a bucket's "
-                                 "CTAs start on the SMs the previous bucket frees"},
-            "clocks": clocks,
-        }
-        if rows is not None:
-            line["rows"] = rows
-        print(json.dumps(line), flush=True)
+        line = headline(value=value, world=world, K=K, W=W, elapsed_ms=elapsed_ms, plan=plan, num=num,
+                        peak=peak, peak_kind=peak_kind, achieved=achieved, avg_launch_ms=avg_launch_ms,
+                        traffic=traffic, traffic_note=traffic_note, cpu=cpu, e2e_copy=e2e_copy,
+                        e2e_zero=e2e_zero, h2d_gbs=h2d_gbs, host_check=host_check,
+                        e2e_steps=args.e2e_steps, clocks=clocks, step_streams=len(bucket_streams))
+        emit_headline(line)
     if world > 1:
         dist.destroy_process_group()
+
+
+HEADLINE_MAX_BYTES = 3500   # the result line stays short: the last line of stdout, read from its tail
+
+
+def headline(*, value, world, K, W, elapsed_ms, plan, num, peak, peak_kind, achieved, avg_launch_ms, traffic,
+             traffic_note, cpu, e2e_copy, e2e_zero, h2d_gbs, host_check, e2e_steps, clocks, step_streams):
+    """The one result line of the run (a flat, short dict): the headline
+    metric, the dominant kernel's roofline, the CPU oracle baseline, the
+    end-to-end figure and the clocks of the timed region."""
+    nb = len(plan["buckets"])
+    step_bytes = algorithmic_bytes(plan)
+    total = plan["total_elems"]
+    cfg = workload_config(plan, num)
+    cfg["schedule"] = f"one CUDA graph per step, each bucket launch on its own stream ({step_streams} streams)"
+    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "peak_source": f"{peak_kind} HBM copy bandwidth",
+            "kernel": "mean_kernel (fp32, rank order, N=8)",
+            "algorithmic_bytes_per_launch": step_bytes / nb, "avg_launch_us": avg_launch_ms * 1e3,
+            "launch_timing": "the step's 5 launches serialised on one stream, K graph replays, CUDA events"}
+    if traffic_note:
+        roof["traffic_note"] = traffic_note
+    if cpu is not None:
+        cpu = {k: v for k, v in cpu.items() if k != "c_oracle"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic: seeded N(0, 0.01) fp32 replica gradients drawn on the device",
+        "config": cfg,
+        "hbm_fraction": value / world / peak,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_copy, "unit": "GB/s", "h2d_bytes_per_step": N_REPLICAS * total * 4,
+                "d2h_bytes_per_step": total * 4, "steps": e2e_steps, "mode": "copy (pinned host <-> HBM, "
+                "pipelined by bucket)", "zero_copy_mode_value": e2e_zero, "modes_agree_bitwise": host_check,
+                "host_link_h2d_GBps": h2d_gbs},
+        "gpu_launches": K * nb,
+        "clocks": clocks,
+    }
+    return line
+
+
+def emit_row(name, row, path=None):
+    """One side measurement as its own JSON line on stdout (and appended to
+    `path` if given), printed before the result line."""
+    rec = {"row": name, **row}
+    s = json.dumps(rec)
+    print(s, flush=True)
+    if path:
+        with open(path, "a", encoding="utf-8") as f:
+            f.write(s + "\n")
+
+
+def emit_headline(line):
+    """Print the result line: the last line of stdout, compact."""
+    s = json.dumps(line, separators=(",", ":"))
+    if len(s) > HEADLINE_MAX_BYTES:
+        raise RuntimeError(f"result line is {len(s)} bytes, over {HEADLINE_MAX_BYTES}")
+    sys.stdout.flush()
+    print(s, flush=True)
 
 
 def _time_launches(torch, fn, iters, stream):
@@ -572,14 +638,15 @@ def _fan_out(torch, calls, streams):
         cur.wait_stream(st)
 
 
-def bench_rows(g, torch, dev, peak, peak_kind, only=None):
+def bench_rows(g, torch, dev, peak, peak_kind, only=None, rows_out=None):
     """The other rows of the hot path, each on its own workload (not part of
     the headline value): fused SGD on GPT-2 small, SyncBN on the four
-    activation shapes, the ImageNet-size sampler, and the bf16 average."""
+    activation shapes, the ImageNet-size sampler, and the bf16 average.
+    Each row is printed as its own JSON line (emit_row) as soon as it is
+    measured."""
     import workloads
     side = torch.cuda.Stream(device=dev)
     pool = [torch.cuda.Stream(device=dev) for _ in range(2)]   # the two GPT-2 buckets are disjoint
-    rows = {}
 
     def want(group):
         return only is None or group in only
@@ -596,11 +663,11 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
         ms = _time_launches(torch, lambda: [g.ddp_bucket_allreduce_sgd(reps_l, theta_l, None, 0.1, 0.0, 0.0)
                                             for _ in range(20)], 10, side) / 20
         nbytes = (4 * 4 + 8) * numel_l
-        rows["sgd_linear_128_10"] = {"workload": "Linear(128,10), 4 fp32 replicas (1,290 elements), average + SGD "
+        emit_row("sgd_linear_128_10", {"workload": "Linear(128,10), 4 fp32 replicas (1,290 elements), average + SGD "
                                                  "lr 0.1 in one launch", "ms": ms, "us": ms * 1e3, "bytes": nbytes,
                                      "GBps": nbytes / ms / 1e6, "frac": None, "launches": 1,
                                      "note": "latency-bound (31 KB per call): the figure is µs per call",
-                                     "calls_per_graph": 20}
+                                     "calls_per_graph": 20}, rows_out)
         del reps_l, theta_l
 
     if want("gpt2"):
@@ -618,9 +685,9 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                 for off, n, _, _ in plan["buckets"]], pool)
         ms = _time_launches(torch, sgd_step, 50, side)
         nbytes = sum((2 * N_REPLICAS + 16) * b[1] for b in plan["buckets"])
-        rows["sgd_gpt2_small"] = {"workload": "GPT-2 small (124,439,808 params), 8 bf16 replicas, DEEP/FIRST buckets, "
+        emit_row("sgd_gpt2_small", {"workload": "GPT-2 small (124,439,808 params), 8 bf16 replicas, DEEP/FIRST buckets, "
                                               "SGD momentum 0.9 wd 1e-4", "ms": ms, "bytes": nbytes,
-                                  "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+                                  "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}, rows_out)
 
         # the same step also writing the bf16 compute copy of θ
         low = torch.empty(total, dtype=torch.bfloat16, device=dev)
@@ -631,9 +698,9 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                 for off, n, _, _ in plan["buckets"]], pool)
         ms = _time_launches(torch, sgd_cast_step, 50, side)
         nbytes = sum((2 * N_REPLICAS + 18) * b[1] for b in plan["buckets"])
-        rows["sgd_cast_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, SGD momentum 0.9 wd 1e-4 plus the "
+        emit_row("sgd_cast_gpt2_small", {"workload": "GPT-2 small, 8 bf16 replicas, SGD momentum 0.9 wd 1e-4 plus the "
                                                    "bf16 copy of θ", "ms": ms, "bytes": nbytes,
-                                       "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+                                       "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 2}, rows_out)
         del low
 
         # bf16 -> fp32 average of the same buckets
@@ -645,9 +712,9 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                              for off, n, _, _ in plan["buckets"]], pool)
         ms = _time_launches(torch, mean_bf16, 50, side)
         nbytes = sum((2 * N_REPLICAS + 4) * b[1] for b in plan["buckets"])
-        rows["mean_bf16_gpt2_small"] = {"workload": "GPT-2 small, 8 bf16 replicas, DEEP/FIRST, average to fp32",
+        emit_row("mean_bf16_gpt2_small", {"workload": "GPT-2 small, 8 bf16 replicas, DEEP/FIRST, average to fp32",
                                         "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
-                                        "frac": nbytes / ms / 1e6 / peak, "launches": 2}
+                                        "frac": nbytes / ms / 1e6 / peak, "launches": 2}, rows_out)
         del reps, theta, buf, outb
 
     if want("accum"):
@@ -659,9 +726,9 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                                          dtype=torch.bfloat16) for r in range(N_REPLICAS)]
         ms = _time_launches(torch, lambda: g.ddp_bucket_accumulate(micro, acc), 20, side)
         nbytes = (2 + 8) * N_REPLICAS * total4
-        rows["accumulate_gpt2_small"] = {"workload": "GPT-2 small, 8 replicas, bf16 micro-step gradient added into "
+        emit_row("accumulate_gpt2_small", {"workload": "GPT-2 small, 8 replicas, bf16 micro-step gradient added into "
                                                      "fp32 accumulators (no_sync)", "ms": ms, "bytes": nbytes,
-                                         "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 1}
+                                         "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "launches": 1}, rows_out)
         del micro
         gavg = torch.empty(total4, device=dev)
         theta = workloads.device_normal((total4,), 0.0, 0.02, workloads.seed_for(3, 99), device=dev)
@@ -679,10 +746,10 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                 for off, n, _, _ in plan4["buckets"]], pool)
         ms = _time_launches(torch, clipped_step, 20, side)
         nbytes = sum(((N_REPLICAS + 1) * 4 + 20) * b[1] for b in plan4["buckets"])
-        rows["clipped_step_gpt2_small"] = {"workload": "GPT-2 small, 8 fp32 accumulated replicas: average with norm "
+        emit_row("clipped_step_gpt2_small", {"workload": "GPT-2 small, 8 fp32 accumulated replicas: average with norm "
                                                        "side output, clip to 1.0, SGD momentum 0.9 wd 1e-4",
                                            "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6,
-                                           "frac": nbytes / ms / 1e6 / peak, "launches": 5}
+                                           "frac": nbytes / ms / 1e6 / peak, "launches": 5}, rows_out)
         del acc, gavg, theta, buf
 
     if want("orders"):
@@ -700,10 +767,10 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                     [x[off:off + n] for x in reps_r], out_r[off:off + n], flags=flag)
                     for off, n, _, _ in plan_r["buckets"]], pool_r)
             ms = _time_launches(torch, ordered, 200, side)
-            rows[f"mean_{name}_order_resnet50"] = {
+            emit_row(f"mean_{name}_order_resnet50", {
                 "workload": f"ResNet-50 step (5 x 25 MiB buckets, 8 fp32 replicas), {name}-order reduction",
                 "ms": ms, "bytes": nbytes, "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-                "launches": len(plan_r["buckets"])}
+                "launches": len(plan_r["buckets"])}, rows_out)
         del reps_r, out_r
 
     if want("syncbn"):
@@ -721,10 +788,10 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
             ms = _time_launches(torch, lambda: [g.syncbn_merge_apply(xs, ys, mean, inv, ws) for _ in range(SYNCBN_CALLS)],
                                 10, side) / SYNCBN_CALLS
             nbytes = 6 * N_REPLICAS * B * C * H * W
-            rows[f"syncbn_{C}x{H}x{W}"] = {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
+            emit_row(f"syncbn_{C}x{H}x{W}", {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
                                            "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
                                            "launches": 3, "calls_per_graph": SYNCBN_CALLS,
-                                           "note": "inputs smaller than L2" if nbytes / 3 < L2_BYTES else ""}
+                                           "note": "inputs smaller than L2" if nbytes / 3 < L2_BYTES else ""}, rows_out)
             del xs, ys
 
     if want("sampler"):
@@ -738,16 +805,15 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
         sm_cycles = max(SAMPLER_WARP_INST["alu"] / 2, SAMPLER_WARP_INST["fmaheavy"] / 2, SAMPLER_WARP_INST["all"] / 4) / 152
         idx_per_s = out.numel() / (ms * 1e-3)
         peak_idx = out.numel() / (sm_cycles / 2.07e9)
-        rows["sampler_imagenet"] = {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
+        emit_row("sampler_imagenet", {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
                                     "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
                                     "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
                                     "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
-                                    "launches": 1, "calls_per_graph": SAMPLER_CALLS}
+                                    "launches": 1, "calls_per_graph": SAMPLER_CALLS}, rows_out)
     if want("sweep"):
         # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point): 1 KiB .. 1 GiB
         # per replica in x4 steps, N in {2, 4, 8, 16}, caps {1, 25, 100} MiB; a cap that does not change the
         # launch count is measured once; the 1 MiB split also as grouped launches (up to 1024 buckets each)
-        sweep = []
         for size in [1 << (10 + 2 * k) for k in range(11)]:
             numel = size // 4
             for n in (2, 4, 8, 16):
@@ -770,10 +836,10 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                             e = min(numel, s0 + ce)
                             g.ddp_bucket_allreduce_mean([x[s0:e] for x in reps], outs[s0:e])
                     ms = _time_launches(torch, flat_step, iters, side)
-                    sweep.append({"bytes_per_replica": size, "replicas": n,
-                                  "cap_mib": cap >> 20 if nl > 1 else "any (one launch)",
-                                  "launches": nl, "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
-                                  "frac": nbytes / ms / 1e6 / peak, "l2": l2})
+                    emit_row("sweep_flat_fp32", {"bytes_per_replica": size, "replicas": n,
+                                                 "cap_mib": cap >> 20 if nl > 1 else "any (one launch)",
+                                                 "launches": nl, "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
+                                                 "frac": nbytes / ms / 1e6 / peak, "l2": l2}, rows_out)
                     if nl > 1 and cap == (1 << 20):
                         bl = [(s0, min(ce, numel - s0)) for s0 in range(0, numel, ce)]
 
@@ -781,13 +847,12 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None):
                             for i in range(0, len(bl), 1024):
                                 g.ddp_bucket_allreduce_mean_multi(reps, bl[i:i + 1024], outs)
                         ms = _time_launches(torch, grouped, iters, side)
-                        sweep.append({"bytes_per_replica": size, "replicas": n, "cap_mib": 1,
-                                      "launches": -(-len(bl) // 1024), "grouped": True, "us": ms * 1e3,
-                                      "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak, "l2": l2})
+                        emit_row("sweep_flat_fp32", {"bytes_per_replica": size, "replicas": n, "cap_mib": 1,
+                                                     "launches": -(-len(bl) // 1024), "grouped": True,
+                                                     "us": ms * 1e3, "GBps": nbytes / ms / 1e6,
+                                                     "frac": nbytes / ms / 1e6 / peak, "l2": l2}, rows_out)
                 del reps, outs
-        rows["sweep_flat_fp32"] = sweep
-    rows["_peak"] = {"hbm_gbs": peak, "source": peak_kind}
-    return rows
+    emit_row("_peak", {"hbm_gbs": peak, "source": peak_kind}, rows_out)
 
 
 def main():

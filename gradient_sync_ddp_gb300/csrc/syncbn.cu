@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
     slice_bounds(a, s, p0, p1);
     const uint64_t run_bytes = static_cast<uint64_t>(Gc) * a.HW * ESZ;
     const uint32_t vslot = static_cast<uint32_t>(a.slot_bytes / 16);
-    pdl_wait_then_release();
+    pdl_wait_then_release();   // must stay the wait-then-release form: the apply reads x before its own wait
     const float K = active ? load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + cl) * a.HW) : 0.0f;
 
     float acc_s = 0.0f, acc_q = 0.0f;
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     const uint32_t e_hi = (static_cast<uint32_t>(HW) * (part + 1)) >> a.tc_log2;
     int cl[CPL];
     float K[CPL], acc_s[CPL], acc_q[CPL];
-    pdl_wait_then_release();
+    pdl_wait_then_release();   // must stay the wait-then-release form: the apply reads x before its own wait
 #pragma unroll
     for (int m = 0; m < CPL; ++m) {
         cl[m] = a.G >= 32 ? lane + 32 * m : lane >> a.tc_log2;
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 5) bn_stats_plane_kernel(const __gri
     const uint32_t units = static_cast<uint32_t>(a.HW / W);                     // vectors per plane
     const uint32_t cpp = (units + kChunkVecs - 1) / kChunkVecs;                  // chunks per plane
     const uint32_t total = static_cast<uint32_t>(p1 - p0) * cpp;
-    pdl_wait_then_release();
+    pdl_wait_then_release();   // must stay the wait-then-release form: the apply reads x before its own wait
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);   // shift: x[0][0, c, 0, 0]
     // one (Σd, Σd²) pair per element position of the vector: each sums one element per vector (as
     // many terms as a per-vector total would), at one add and one fused multiply-add per element,
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_element_kernel(const __grid
     const int c = blockIdx.x, s = blockIdx.y;
     int p0, p1;
     slice_bounds(a, s, p0, p1);
-    pdl_wait_then_release();
+    pdl_wait_then_release();   // must stay the wait-then-release form: the apply reads x before its own wait
     const float K = load_elem<BF16>(a.x[0], static_cast<int64_t>(c) * a.HW);
     float acc_s = 0.0f, acc_q = 0.0f;
     for (int pl = p0; pl < p1; ++pl) {
@@ -1153,7 +1153,10 @@ void* g_scratch_addr[kMaxScratchDevices] = {};
 
 // Device address of g_syncbn_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
+// per device (with that device current) and cached for the life of the
+// process.  A cudaDeviceReset of that device leaves the cached address stale
+// (the module is loaded again into a new context), so this entry point is not
+// for processes that reset a device and keep using it.
 int static_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1186,6 +1189,7 @@ extern "C" int syncbn_merge_apply_noalloc(const void* const* x, int32_t n_replic
     void* ws = nullptr;
     const int st = ddp::static_scratch(&ws);
     if (st != DDP_OK) return st;
+    // only the bytes this call needs are handed on, so the capacity and overlap checks cover exactly those
     return syncbn_merge_apply(x, n_replicas, in_dtype, batch, C, H, W, eps, gamma, beta, y, out_dtype, mean_out,
-                              invstd_out, ws, ddp::kStaticScratchBytes, stream);
+                              invstd_out, ws, need, stream);
 }

@@ -423,7 +423,14 @@ int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtyp
  *   with C <= 43690 fits; C <= 2048 needs at most 544 KiB).
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress, with that device current) and caches it;
- *   make that first call before any stream capture.
+ *   make that first call before any stream capture.  The address stays
+ *   cached for the life of the process: after a cudaDeviceReset of that
+ *   device it is stale (the module is loaded again into the new context),
+ *   so a process that resets a device must not call this entry point on it
+ *   again; it can use syncbn_merge_apply with a workspace instead.
+ *   The capacity and overlap checks of syncbn_merge_apply apply to the
+ *   syncbn_workspace_bytes(...) bytes at the start of the array that the
+ *   call uses.
  *   Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents (nothing in it needs to start at zero).  Calls whose
  *   kernels overlap on the GPU (different streams without ordering between

@@ -36,5 +36,6 @@ from .ddp_oracle import (  # noqa: F401
     splitmix64_mix,
     splitmix64_stream,
     syncbn,
+    syncbn_stats,
     syncbn_stats_at,
 )

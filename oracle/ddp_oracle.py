@@ -269,27 +269,39 @@ def syncbn(xs, eps: float = 1e-5, gamma=None, beta=None, dtype: str = "bf16"):
         y_r = (x_r − mean) * invstd * γ + β
     γ defaults to 1 and β to 0 (the pages give neither).
     Returns (mean[C], invstd[C], [y_r]) all fp64."""
-    xs64 = []
-    for x in xs:
-        x = np.asarray(x)
-        xs64.append(bf16_bits_to_f32(x).astype(np.float64) if dtype == "bf16"
-                    else np.asarray(x, dtype=np.float64))
-    C = xs64[0].shape[1]
-    S = np.zeros(C)
-    Q = np.zeros(C)
+    mean, invstd = syncbn_stats(xs, eps, dtype)
+    C = mean.shape[0]
+    g = np.ones(C) if gamma is None else np.asarray(gamma, dtype=np.float64)
+    b = np.zeros(C) if beta is None else np.asarray(beta, dtype=np.float64)
+    ys = [(_to_f64(x, dtype) - mean[None, :, None, None]) * invstd[None, :, None, None] * g[None, :, None, None]
+          + b[None, :, None, None] for x in xs]
+    return mean, invstd, ys
+
+
+def _to_f64(x, dtype):
+    x = np.asarray(x)
+    return bf16_bits_to_f32(x).astype(np.float64) if dtype == "bf16" else np.asarray(x, dtype=np.float64)
+
+
+def syncbn_stats(xs, eps: float = 1e-5, dtype: str = "bf16"):
+    """The merged statistics of ``syncbn`` for every channel: per replica r
+    the fp64 sums s_r[c] = Σ x_r[:, c] and q_r[c] = Σ x_r[:, c]^2 over its
+    B*H*W elements ([TR24] §十二: each rank's sum and sum of squares), then
+    S = Σ_r s_r, Q = Σ_r q_r, M = Σ_r n_r, mean = S/M,
+    var = Q/M − mean^2, invstd = 1/sqrt(var + eps).  One replica is widened
+    to fp64 at a time, so full-size inputs fit in host memory.
+    Returns (mean[C], invstd[C]) fp64."""
+    S = Q = None
     M = 0
-    for x in xs64:
-        S += x.sum(axis=(0, 2, 3))
-        Q += (x * x).sum(axis=(0, 2, 3))
+    for x in xs:
+        x = _to_f64(x, dtype)
+        s, q = x.sum(axis=(0, 2, 3)), (x * x).sum(axis=(0, 2, 3))
+        S = s if S is None else S + s
+        Q = q if Q is None else Q + q
         M += x.shape[0] * x.shape[2] * x.shape[3]
     mean = S / M
     var = Q / M - mean * mean
-    invstd = 1.0 / np.sqrt(var + eps)
-    g = np.ones(C) if gamma is None else np.asarray(gamma, dtype=np.float64)
-    b = np.zeros(C) if beta is None else np.asarray(beta, dtype=np.float64)
-    ys = [(x - mean[None, :, None, None]) * invstd[None, :, None, None] * g[None, :, None, None]
-          + b[None, :, None, None] for x in xs64]
-    return mean, invstd, ys
+    return mean, 1.0 / np.sqrt(var + eps)
 
 
 def syncbn_stats_at(xs, c: int, eps: float = 1e-5, dtype: str = "bf16"):

@@ -1,12 +1,25 @@
 """GPU parity: syncbn_merge_apply against the fp64 oracle.
 
-Tolerances (the computation is not bit-reproducible by design: fp32 partial
-sums, float-float merge, fp32 apply):
-  mean, invstd       |gpu − oracle| <= 1e-5 · |oracle| (+1e-7 absolute for a mean near 0)
+Tolerances (the computation is not bit-reproducible against fp64 by design:
+fp32 partial sums, float-float merge, fp32 apply):
+  mean               |gpu − oracle| <= 1e-5 · |oracle| + 1e-7 · σ_c
+  invstd             |gpu − oracle| <= 1e-5 · |oracle|
   y (fp32 output)    |gpu − oracle| <= 1e-5 · |oracle| + 1e-6
   y (bf16 output)    within one bf16 ulp of the oracle's fp64 value rounded to
                      bf16, plus the fp32 allowance above (the fp32 result
                      may sit on the other side of a bf16 rounding boundary)
+σ_c = 1/invstd_c is the channel's standard deviation.  The GPU sums x − K_c
+in fp32, so its mean carries an absolute error of the order of the fp32
+unit roundoff (6e-8) times the spread of the summed values, whatever the
+mean: no relative bound can hold for a channel whose mean is near zero
+(some test channels have means of 0.002 with σ_c = 2).  1e-7 · σ_c is
+stricter than y needs: an error δ in the mean moves y by δ · invstd, and
+y's absolute allowance of 1e-6 admits δ up to 1e-6 · σ_c.
+The 1e-6 absolute term of y covers outputs near zero (x near the mean),
+where a relative bound means nothing: there y's error is the fp32 rounding
+of the shift β − m_lo·scale plus the mean's error times invstd·γ, both far
+below 1e-6 for the inputs here (means of 0.5 or 1000 and standard
+deviations of 2 or 0.1 computed to about 1e-7 relative).
 """
 import numpy as np
 import pytest
@@ -33,7 +46,7 @@ def _bf16_ulp(v):
 def _check_stats(mean, invstd, m_w, s_w, what):
     m = mean.cpu().numpy().astype(np.float64)
     s = invstd.cpu().numpy().astype(np.float64)
-    assert np.all(np.abs(m - m_w) <= 1e-5 * np.abs(m_w) + 1e-7), what
+    assert np.all(np.abs(m - m_w) <= 1e-5 * np.abs(m_w) + 1e-7 / s_w), what
     assert np.all(np.abs(s - s_w) <= 1e-5 * np.abs(s_w)), what
 
 
@@ -123,31 +136,28 @@ def test_constant_channel(g):
 
 
 @pytest.mark.parametrize("C,H,W", workloads.SYNCBN_SHAPES)
-def test_full_size_shapes_sampled(g, C, H, W):
-    """N = 8 replicas x [32, C, H, W] bf16 drawn N(0.5, 2) on the device.
-    Checked: mean/invstd of 16 channels spread over C (oracle over every
-    element of those channels), and y at 2^16 random positions of those
-    channels in every replica."""
+def test_full_size_shapes(g, C, H, W):
+    """N = 8 replicas x [32, C, H, W] bf16 drawn N(0.5, 2) on the device, in
+    the launch configuration the benchmark times.  Checked: mean and invstd
+    of every channel against the fp64 oracle over every element, and y at
+    2^16 random positions of every replica (all channels)."""
     n, B = 8, workloads.SYNCBN_BATCH
     xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, workloads.seed_for(4, r), dtype=torch.bfloat16)
           for r in range(n)]
     ys = [torch.empty_like(x) for x in xs]
     mean, invstd = _run(g, xs, ys, C)
-    chans = np.unique(np.linspace(0, C - 1, 16).astype(np.int64))
+    xh = [x.view(torch.int16).cpu().numpy().view(np.uint16) for x in xs]
+    m_w, s_w = oracle.syncbn_stats(xh, 1e-5)
+    _check_stats(mean, invstd, m_w, s_w, f"C={C} H={H} W={W}")
     gen = np.random.Generator(np.random.PCG64(C))
-    m_all, s_all = mean.cpu().numpy(), invstd.cpu().numpy()
-    for c in chans:
-        xc = [x[:, c].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)[:, None] for x in xs]
-        m_w, s_w = oracle.syncbn_stats_at(xc, 0, 1e-5)
-        assert abs(m_all[c] - m_w) <= 1e-5 * abs(m_w) + 1e-7, (c, m_all[c], m_w)
-        assert abs(s_all[c] - s_w) <= 1e-5 * s_w, (c, s_all[c], s_w)
-        for r in range(n):
-            b = gen.integers(0, B, 4096)
-            hw = gen.integers(0, H * W, 4096)
-            xv = oracle.bf16_bits_to_f32(xc[r][:, 0].reshape(B, H * W)[b, hw]).astype(np.float64)
-            y_w = (xv - m_w) * s_w
-            got = ys[r][:, c].reshape(B, H * W)[torch.from_numpy(b).cuda(), torch.from_numpy(hw).cuda()]
-            _check_y(got, y_w, f"C={C} c={c} r={r}")
+    E = B * C * H * W
+    for r in range(n):
+        pos = gen.integers(0, E, 1 << 16)
+        c = (pos // (H * W)) % C
+        xv = oracle.bf16_bits_to_f32(xh[r].reshape(-1)[pos]).astype(np.float64)
+        y_w = (xv - m_w[c]) * s_w[c]
+        got = ys[r].reshape(-1)[torch.from_numpy(pos).cuda()]
+        _check_y(got, y_w, f"C={C} H={H} W={W} r={r}")
 
 
 def test_large_mean_small_std(g):
@@ -160,15 +170,15 @@ def test_large_mean_small_std(g):
     mean, invstd = _run(g, [dev_f32(x) for x in xs], ys, C)
     m_w, s_w, y_w = oracle.syncbn(xs, 1e-5, dtype="f32")
     _check_stats(mean, invstd, m_w, s_w, "large mean")
+    # x − m_hi is exact (both within a factor of two of 1000) and the mean's low part goes into the
+    # shift, so y keeps the ordinary fp32 tolerance although invstd ≈ 10 magnifies any error in the mean
     for r in range(n):
-        got = ys[r].cpu().numpy().astype(np.float64)
-        # x − mean is exact in fp32 near 1000 only to ~6e-5 absolute (fp32 spacing of the input
-        # itself): y inherits that times invstd ≈ 10, so compare with 1e-3 absolute here
-        assert np.all(np.abs(got - y_w[r]) <= 1e-5 * np.abs(y_w[r]) + 1e-3)
+        _check_y(ys[r], y_w[r], f"large mean y[{r}]")
 
 
 @pytest.mark.parametrize("shape,in_place", [((8, 32, 128, 28, 28), False), ((8, 32, 256, 14, 14), False),
-                                            ((8, 32, 128, 28, 28), True)])
+                                            ((8, 32, 128, 28, 28), True), ((8, 32, 256, 14, 14), True),
+                                            ((8, 32, 2048, 7, 7), True)])
 def test_chained_layers_equal_separate_calls(g, shape, in_place):
     """Three SyncBN calls back to back on one stream, each reading the
     previous call's output: a call's apply reads its first vectors of x
@@ -225,7 +235,7 @@ def test_non_finite_channel_stays_in_its_channel(g, shape):
         assert not (np.isfinite(m_w[c]) and np.isfinite(s_w[c]))
         assert not (np.isfinite(m[c]) and np.isfinite(s[c])), (c, m[c], s[c])
     good = [c for c in range(C) if c not in bad]
-    assert np.all(np.abs(m[good] - m_w[good]) <= 1e-5 * np.abs(m_w[good]) + 1e-7)
+    assert np.all(np.abs(m[good] - m_w[good]) <= 1e-5 * np.abs(m_w[good]) + 1e-7 / s_w[good])
     assert np.all(np.abs(s[good] - s_w[good]) <= 1e-5 * np.abs(s_w[good]))
     for r in range(n):
         _check_y(ys[r][:, good], np.asarray(y_w[r])[:, good], f"{shape} y[{r}] finite channels")
