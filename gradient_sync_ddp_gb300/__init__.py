@@ -411,6 +411,8 @@ _lib.ddp_reducer_reset.argtypes = [_P]
 _lib.ddp_reducer_reset.restype = _c.c_int
 _lib.ddp_reducer_completed.argtypes = [_P, _P, _c.c_int32, _P]
 _lib.ddp_reducer_completed.restype = _c.c_int
+_lib.ddp_reducer_take_ready.argtypes = [_P, _c.c_int64, _P, _c.c_int32, _P]
+_lib.ddp_reducer_take_ready.restype = _c.c_int
 
 
 def ddp_reducer_create(tensor_bucket, n_buckets: int) -> int:
@@ -466,8 +468,19 @@ def ddp_reducer_completed(handle) -> list:
     return list(arr[:n.value])
 
 
+def ddp_reducer_take_ready(handle, timeout_us: int = 0, max_out: int = MULTI_MAX_BUCKETS) -> list:
+    """Buckets completed since the previous take, in bucket order (waits up
+    to timeout_us for one if none is waiting); each is taken once per
+    iteration."""
+    arr = (ctypes.c_int32 * max(1, max_out))()
+    n = ctypes.c_int32(0)
+    _check(_lib.ddp_reducer_take_ready(handle, int(timeout_us), ctypes.addressof(arr), max_out,
+                                       ctypes.addressof(n)), "ddp_reducer_take_ready")
+    return list(arr[:n.value])
+
+
 __all__ += ["ddp_reducer_create", "ddp_reducer_destroy", "ddp_reducer_mark_ready", "ddp_reducer_mark_unused",
-            "ddp_reducer_wait_all", "ddp_reducer_reset", "ddp_reducer_completed"]
+            "ddp_reducer_wait_all", "ddp_reducer_reset", "ddp_reducer_completed", "ddp_reducer_take_ready"]
 
 
 # ---------------------------------------------------------------- sampler resume

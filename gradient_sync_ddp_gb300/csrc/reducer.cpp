@@ -9,9 +9,14 @@
 // (find_unused_parameters).  Here the wait is bounded and the parameter that
 // was never marked is reported.
 //
+// §3.2 also has buckets fire as they fill; when hooks complete several
+// buckets faster than the caller launches them (the end of backward, small
+// caps), ddp_reducer_take_ready hands over every bucket completed since the
+// previous take at once, so they can go out as one grouped launch.
+//
 // Host code only.  One mutex guards the state; a condition variable wakes
-// ddp_reducer_wait_all when a bucket completes.  Marking is O(1): each bucket
-// keeps the number of parameters still missing.
+// ddp_reducer_wait_all and ddp_reducer_take_ready when a bucket completes.
+// Marking is O(1): each bucket keeps the number of parameters still missing.
 #include <chrono>
 #include <condition_variable>
 #include <cstdint>
@@ -29,6 +34,8 @@ struct ddp_reducer {
     std::vector<int32_t> missing;         // parameters not yet marked, per bucket
     std::vector<uint8_t> marked;          // per parameter: 0 no, 1 ready, 2 unused
     std::vector<int32_t> done_order;      // buckets completed this iteration, in order
+    std::vector<uint8_t> taken;           // per bucket: handed out by ddp_reducer_take_ready
+    int32_t n_taken = 0;                  // buckets handed out this iteration
     int32_t buckets_left = 0;
 };
 
@@ -45,7 +52,8 @@ int mark(ddp_reducer* r, int32_t tensor, int32_t* bucket_done, uint8_t how) {
     if (--r->missing[b] == 0) {
         *bucket_done = b;
         r->done_order.push_back(b);
-        if (--r->buckets_left == 0) r->cv.notify_all();
+        --r->buckets_left;
+        r->cv.notify_all();
     }
     return DDP_OK;
 }
@@ -73,6 +81,7 @@ extern "C" int ddp_reducer_create(int32_t n_tensors, const int32_t* tensor_bucke
     r->missing = size;
     r->marked.assign(static_cast<size_t>(n_tensors), 0);
     r->done_order.reserve(static_cast<size_t>(n_buckets));
+    r->taken.assign(static_cast<size_t>(n_buckets), 0);
     r->buckets_left = n_buckets;
     *out = r;
     return DDP_OK;
@@ -109,7 +118,32 @@ extern "C" int ddp_reducer_reset(ddp_reducer* r) {
     r->missing = r->bucket_size;
     r->marked.assign(r->marked.size(), 0);
     r->done_order.clear();
+    r->taken.assign(r->taken.size(), 0);
+    r->n_taken = 0;
     r->buckets_left = static_cast<int32_t>(r->bucket_size.size());
+    return DDP_OK;
+}
+
+extern "C" int ddp_reducer_take_ready(ddp_reducer* r, int64_t timeout_us, int32_t* buckets_out, int32_t max_out,
+                                      int32_t* n_out) {
+    if (r == nullptr || n_out == nullptr || buckets_out == nullptr || max_out < 1 || timeout_us < 0)
+        return DDP_ERR_INVALID_ARG;
+    std::unique_lock<std::mutex> lock(r->mu);
+    const int32_t nb = static_cast<int32_t>(r->bucket_size.size());
+    auto pending = [r] { return static_cast<int32_t>(r->done_order.size()) > r->n_taken; };
+    // wait for a completed bucket not yet handed out, unless every bucket has been handed out already
+    if (!pending() && r->n_taken < nb && timeout_us > 0)
+        r->cv.wait_for(lock, std::chrono::microseconds(timeout_us), [&] { return pending(); });
+    // completed, not yet handed out: in bucket index order (a plan's offset order), lowest first
+    int32_t n = 0;
+    for (int32_t b = 0; b < nb && n < max_out; ++b) {
+        if (r->missing[b] == 0 && !r->taken[b]) {
+            r->taken[b] = 1;
+            buckets_out[n++] = b;
+        }
+    }
+    r->n_taken += n;
+    *n_out = n;
     return DDP_OK;
 }
 

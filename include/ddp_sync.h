@@ -186,6 +186,33 @@ int ddp_reducer_reset(ddp_reducer* r);
 int ddp_reducer_completed(const ddp_reducer* r, int32_t* order_out, int32_t max_out, int32_t* n_done);
 
 /*
+ * ddp_reducer_take_ready — every bucket that completed since the previous
+ * take (or since create / reset), for one grouped launch.
+ *
+ * [DDP] §3.2: buckets fire as they fill.  When hooks complete buckets faster
+ * than the caller launches them (the end of backward; small caps, where one
+ * launch per bucket is latency-bound), the caller takes all the completed
+ * buckets at once and averages them with one
+ * ddp_bucket_allreduce_mean_multi call instead of one call per bucket.
+ *   timeout_us   >= 0: if no completed bucket is waiting, wait up to this
+ *                long for one (0: do not wait); no wait once every bucket of
+ *                the iteration has been taken
+ *   buckets_out  host int32[max_out] (max_out >= 1): the buckets taken, in
+ *                increasing bucket index order (a plan's offset order, as
+ *                ddp_bucket_allreduce_mean_multi wants); when more than
+ *                max_out are waiting, the lowest max_out are taken and the
+ *                rest stay for the next take
+ *   n_out        receives the number taken (0 when the wait ran out, or
+ *                when every bucket has been taken)
+ * Each bucket is taken exactly once per iteration.  The bucket_done result
+ * of the mark calls is independent of taking: a caller uses one or the
+ * other to decide what to launch.
+ * DDP_ERR_INVALID_ARG on a NULL pointer, max_out < 1 or timeout_us < 0.
+ */
+int ddp_reducer_take_ready(ddp_reducer* r, int64_t timeout_us, int32_t* buckets_out, int32_t max_out,
+                           int32_t* n_out);
+
+/*
  * ddp_bucket_allreduce_mean — average one bucket over N replicas.
  *
  * [TR24] §一: grad_sync = 0; for r in 0..N-1: grad_sync += grad[r];

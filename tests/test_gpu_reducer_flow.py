@@ -136,3 +136,47 @@ def test_skipped_layer_times_out_until_marked_unused(g):
         f.check("averages with the skipped layer zeroed")
     finally:
         g.ddp_reducer_destroy(f.h)
+
+
+def test_buckets_completed_together_go_out_in_one_grouped_launch(g):
+    """Small caps (4 KiB: six buckets for this model) make one launch per
+    bucket latency-bound.  Here the hooks only copy and mark; the first
+    time three or more buckets are complete, the hook takes every completed
+    bucket from the tracker and averages them with one grouped launch
+    (ddp_bucket_allreduce_mean_multi); after backward the rest go out the
+    same way.  Every bucket is launched exactly once, at least one launch
+    carries several buckets, and the averages equal the oracle's bit for
+    bit."""
+    f = Flow(g, cap_bytes=4 << 10)
+    groups = []
+
+    def launch_group(bs):
+        if not bs:
+            return
+        ev = torch.cuda.Event()
+        ev.record(torch.cuda.current_stream())
+        f.side.wait_event(ev)
+        g.ddp_bucket_allreduce_mean_multi(f.flat, [f.plan["buckets"][b] for b in bs], f.out, stream=f.side)
+        groups.append(bs)
+
+    def ready(r, t, p):
+        off, numel = f.plan["tensor_offset"][t], p.numel()
+        f.flat[r][off:off + numel].copy_(p.grad.reshape(-1))
+        g.ddp_reducer_mark_ready(f.h, r * f.T + t)
+        if not groups and len(g.ddp_reducer_completed(f.h)) >= 3:
+            launch_group(g.ddp_reducer_take_ready(f.h))
+
+    f.ready = ready
+    try:
+        nb = len(f.plan["buckets"])
+        assert nb >= 4
+        f.backward()
+        assert g.ddp_reducer_wait_all(f.h, 2_000_000) == (True, -1)
+        launch_group(g.ddp_reducer_take_ready(f.h))
+        sync()
+        assert sorted(b for grp in groups for b in grp) == list(range(nb))
+        assert max(len(grp) for grp in groups) >= 3
+        assert all(grp == sorted(grp) for grp in groups)
+        f.check("grouped launches of the completed buckets")
+    finally:
+        g.ddp_reducer_destroy(f.h)

@@ -176,3 +176,113 @@ def test_hook_thread_that_never_fires(g):
         assert sorted(g.ddp_reducer_completed(h)) == [0, 1, 3]
     finally:
         g.ddp_reducer_destroy(h)
+
+
+def test_take_ready_groups_buckets_completed_together(g):
+    """ddp_reducer_take_ready hands over every bucket completed since the
+    previous take, in bucket order, each once per iteration ([DDP] §3.2:
+    buckets fire as they fill; buckets that fill together go out together)."""
+    plan, tb, h = _resnet_tracker(g)
+    try:
+        T, B = len(tb), len(plan["buckets"])
+        assert B == 5
+        order = list(reversed(range(T)))                      # backward order
+        last = {b: min(t for t in range(T) if tb[t] == b) for b in range(B)}
+        i = 0
+        for t in order:                                       # complete buckets 0, 1 and 2 without taking
+            g.ddp_reducer_mark_ready(h, t)
+            i += 1
+            if t == last[2]:
+                break
+        assert g.ddp_reducer_take_ready(h) == [0, 1, 2]
+        assert g.ddp_reducer_take_ready(h) == []              # nothing new; timeout 0 does not wait
+        for t in order[i:]:
+            g.ddp_reducer_mark_ready(h, t)
+        assert g.ddp_reducer_take_ready(h, max_out=1) == [3]  # the lowest first, the rest stays
+        assert g.ddp_reducer_take_ready(h) == [4]
+        t0 = time.monotonic()
+        assert g.ddp_reducer_take_ready(h, 5_000_000) == []   # every bucket taken: returns at once
+        assert time.monotonic() - t0 < 1.0
+        g.ddp_reducer_reset(h)                                # a new iteration: nothing taken, nothing ready
+        assert g.ddp_reducer_take_ready(h, 20_000) == []
+        for t in order:
+            g.ddp_reducer_mark_ready(h, t)
+        assert g.ddp_reducer_take_ready(h) == list(range(B))
+    finally:
+        g.ddp_reducer_destroy(h)
+
+
+def test_take_ready_random_marks_and_takes(g):
+    """Random marking order with takes at random points: every take is
+    sorted, holds only buckets complete at that moment and not taken
+    before; together the takes hold every bucket exactly once."""
+    gen = np.random.Generator(np.random.PCG64(11))
+    for trial in range(30):
+        T = int(gen.integers(1, 60))
+        B = int(gen.integers(1, T + 1))
+        tb = list(gen.permutation(np.concatenate([np.arange(B), gen.integers(0, B, T - B)])).astype(int))
+        h = g.ddp_reducer_create(tb, B)
+        try:
+            missing = {b: {t for t in range(T) if tb[t] == b} for b in range(B)}
+            taken = []
+            for t in gen.permutation(T):
+                g.ddp_reducer_mark_ready(h, int(t))
+                missing[tb[t]].discard(int(t))
+                if gen.random() < 0.3:
+                    got = g.ddp_reducer_take_ready(h, max_out=int(gen.integers(1, 4)))
+                    assert got == sorted(got)
+                    assert all(not missing[b] and b not in taken for b in got)
+                    taken += got
+            while True:
+                got = g.ddp_reducer_take_ready(h)
+                if not got:
+                    break
+                taken += got
+            assert sorted(taken) == list(range(B))
+        finally:
+            g.ddp_reducer_destroy(h)
+
+
+def test_take_ready_launcher_thread(g):
+    """Hooks mark on 4 threads; a launcher thread takes with a bounded wait
+    until it has every bucket.  Each bucket reaches the launcher once."""
+    plan, tb, h = _resnet_tracker(g)
+    try:
+        T, B = len(tb), len(plan["buckets"])
+        got = []
+
+        def launcher():
+            deadline = time.monotonic() + 20
+            while len(got) < B and time.monotonic() < deadline:
+                got.extend(g.ddp_reducer_take_ready(h, 100_000))
+
+        def marker(k):
+            for t in range(k, T, 4):
+                g.ddp_reducer_mark_ready(h, t)
+        lt = threading.Thread(target=launcher)
+        lt.start()
+        ms = [threading.Thread(target=marker, args=(k,)) for k in range(4)]
+        for m in ms:
+            m.start()
+        for m in ms:
+            m.join()
+        lt.join(timeout=30)
+        assert sorted(got) == list(range(B))
+    finally:
+        g.ddp_reducer_destroy(h)
+
+
+def test_take_ready_rejects(g):
+    h = g.ddp_reducer_create([0, 1], 2)
+    try:
+        lib = g.lib_handle()
+        import ctypes
+        buf = (ctypes.c_int32 * 2)()
+        n = ctypes.c_int32(0)
+        assert lib.ddp_reducer_take_ready(h, 0, ctypes.addressof(buf), 0, ctypes.addressof(n)) == g.DDP_ERR_INVALID_ARG
+        assert lib.ddp_reducer_take_ready(h, -1, ctypes.addressof(buf), 2, ctypes.addressof(n)) == g.DDP_ERR_INVALID_ARG
+        assert lib.ddp_reducer_take_ready(h, 0, None, 2, ctypes.addressof(n)) == g.DDP_ERR_INVALID_ARG
+        assert lib.ddp_reducer_take_ready(h, 0, ctypes.addressof(buf), 2, None) == g.DDP_ERR_INVALID_ARG
+        assert lib.ddp_reducer_take_ready(None, 0, ctypes.addressof(buf), 2, ctypes.addressof(n)) == g.DDP_ERR_INVALID_ARG
+    finally:
+        g.ddp_reducer_destroy(h)
