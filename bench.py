@@ -44,13 +44,21 @@ CAP_BYTES = 25 * MiB
 METRIC = "bucket allreduce-mean GB/s (HBM bytes moved) & % of HBM roofline, 1×GB300"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 10 ** 6
-# Warp instructions one sampler launch issues on the ImageNet-size workload (1,281,168 output
-# slots), by pipe, from an ncu capture of this launch.  The integer ALU and the FMA-heavy
-# pipe each take 2 warp instructions per SM cycle; the four schedulers issue 4 per SM cycle.
+# Sampler roofline (integer arithmetic; the 8 bytes written per index are far below HBM's rate).
+# One encryption of the keyed permutation is 4 Feistel rounds, each the MurmurHash3 32-bit
+# finalizer of (half xor round key) masked and xored into the other half: 2 multiplies, 3 shifts
+# and 6 logic operations; the cycle walk then composes the value (1 multiply-add) and compares it
+# with n (1): 46 integer operations per encryption.  Cycle walking takes 2^bits / n encryptions per
+# index on average (bits = ceil(log2 n): the domain over the values in range).  Each SM issues 4
+# warp instructions (128 lanes) per cycle, and its two integer-capable pipes (ALU: logic, shifts,
+# compares; FMA-heavy: multiplies, and shifts written as multiply-highs) take 64 lanes per cycle
+# each: at best 128 integer operations per SM cycle.
+SAMPLER_OPS_PER_ENCRYPTION = 4 * (2 + 3 + 6) + 2
+SAMPLER_OPS_PER_SM_CYCLE = 128
+GB300_SMS = 152
 STEP_STREAMS = 8       # streams the headline step's bucket launches are spread over
-SYNCBN_CALLS = 10      # calls captured per graph in the SyncBN rows
+SYNCBN_CALLS = 12      # calls captured per graph in the SyncBN rows (a multiple of every input-set count)
 SAMPLER_CALLS = 20     # calls (epochs 1..20) captured per graph in the sampler row
-SAMPLER_WARP_INST = {"alu": 2_712_355, "fmaheavy": 2_149_134, "all": 6_251_798}
 
 
 def parse_args():
@@ -774,25 +782,33 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None, rows_out=None):
         del reps_r, out_r
 
     if want("syncbn"):
-        # SyncBN, 4 shapes
+        # SyncBN, 4 shapes.  Calls cycle through R input sets (each set: 8 replicas' x and y) with
+        # R·(x + y) >= 2.5 x L2, so a call never finds its x left in L2 by an earlier call: the stats
+        # pass reads x from HBM.  (Within one call the apply's second read of x may still hit L2 when x
+        # is smaller than L2; the bytes counted stay the algorithmic 6 per element.)
         for C, H, W in workloads.SYNCBN_SHAPES:
             B = workloads.SYNCBN_BATCH
-            xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, workloads.seed_for(4, r), device=dev,
-                                          dtype=torch.bfloat16) for r in range(N_REPLICAS)]
-            ys = [torch.empty_like(x) for x in xs]
+            xbytes = 2 * N_REPLICAS * B * C * H * W
+            R = max(1, -(-int(2.5 * L2_BYTES) // (2 * xbytes)))
+            sets = []
+            for k in range(R):
+                xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, workloads.seed_for(4, r) + 100 * k, device=dev,
+                                              dtype=torch.bfloat16) for r in range(N_REPLICAS)]
+                sets.append((xs, [torch.empty_like(x) for x in xs]))
             ws = torch.empty(g.syncbn_workspace_bytes(N_REPLICAS, B, C, H, W), dtype=torch.uint8, device=dev)
             mean = torch.empty(C, device=dev)
             inv = torch.empty(C, device=dev)
             # SYNCBN_CALLS back-to-back calls per graph replay (as consecutive BN layers sit in a captured
             # step), so the figure is device time per call, not one graph launch's latency per call
-            ms = _time_launches(torch, lambda: [g.syncbn_merge_apply(xs, ys, mean, inv, ws) for _ in range(SYNCBN_CALLS)],
-                                10, side) / SYNCBN_CALLS
+            ms = _time_launches(torch, lambda: [g.syncbn_merge_apply(*sets[i % R], mean, inv, ws)
+                                                for i in range(SYNCBN_CALLS)], 10, side) / SYNCBN_CALLS
             nbytes = 6 * N_REPLICAS * B * C * H * W
             emit_row(f"syncbn_{C}x{H}x{W}", {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
                                            "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-                                           "launches": 3, "calls_per_graph": SYNCBN_CALLS,
-                                           "note": "inputs smaller than L2" if nbytes / 3 < L2_BYTES else ""}, rows_out)
-            del xs, ys
+                                           "launches": 3, "calls_per_graph": SYNCBN_CALLS, "input_sets": R,
+                                           "l2": f"{R} input sets rotated: {R * 2 * xbytes / 1e6:.0f} MB of x and y "
+                                                 f"against {L2_BYTES / 1e6:.0f} MB of L2"}, rows_out)
+            del sets
 
     if want("sampler"):
         # sampler
@@ -800,16 +816,20 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None, rows_out=None):
         out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
         ms = _time_launches(torch, lambda: [g.dist_sampler_indices(n, N, -1, 0, 1 + e, True, False, out)
                                             for e in range(SAMPLER_CALLS)], 10, side) / SAMPLER_CALLS
-        # Integer-pipe roofline: the launch's measured instruction stream at full issue -- the slowest of
-        # ALU pipe (2 / SM cycle), FMA-heavy pipe (2 / SM cycle) and issue (4 / SM cycle), 152 SMs, 2.07 GHz
-        sm_cycles = max(SAMPLER_WARP_INST["alu"] / 2, SAMPLER_WARP_INST["fmaheavy"] / 2, SAMPLER_WARP_INST["all"] / 4) / 152
+        # Integer roofline from the arithmetic (SAMPLER_OPS_PER_ENCRYPTION), at the maximum SM clock
+        bits = max(1, (n - 1).bit_length())
+        enc_per_index = (1 << bits) / n
+        sm_hz = 2.07e9
+        peak_idx = GB300_SMS * SAMPLER_OPS_PER_SM_CYCLE * sm_hz / (SAMPLER_OPS_PER_ENCRYPTION * enc_per_index)
         idx_per_s = out.numel() / (ms * 1e-3)
-        peak_idx = out.numel() / (sm_cycles / 2.07e9)
         emit_row("sampler_imagenet", {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
-                                    "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
-                                    "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
-                                    "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
-                                    "launches": 1, "calls_per_graph": SAMPLER_CALLS}, rows_out)
+                                      "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
+                                      "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
+                                      "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
+                                      "peak_basis": f"{SAMPLER_OPS_PER_ENCRYPTION} integer ops per encryption x "
+                                                    f"{enc_per_index:.4f} encryptions per index; {GB300_SMS} SMs x "
+                                                    f"{SAMPLER_OPS_PER_SM_CYCLE} ops per cycle at 2070 MHz",
+                                      "launches": 1, "calls_per_graph": SAMPLER_CALLS}, rows_out)
     if want("sweep"):
         # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point): 1 KiB .. 1 GiB
         # per replica in x4 steps, N in {2, 4, 8, 16}, caps {1, 25, 100} MiB; a cap that does not change the
