@@ -41,12 +41,18 @@
 //      m_hi + m_lo and scale = invstd·γ, it stores per channel (m_hi, scale,
 //      shift), shift = β − m_lo·scale rounded once.
 //   3. apply  — y = (x − m_hi)·scale + shift over every replica, 16-byte
-//      vectors in and out, the channel computed once per 8-element vector,
-//      element pairs in packed f32x2 arithmetic.  x − m_hi is exact when x
-//      is near the mean (Sterbenz), so no cancellation error is amplified
-//      by a large invstd; only the mean's tiny low part goes into the shift
-//      (the form x·scale + (β − mean·scale) would lose that protection).
+//      vectors in and out, the channel computed once per 8-element vector
+//      (or, where the grid stride is a whole number of samples, once per
+//      thread), element pairs in packed f32x2 arithmetic.  x − m_hi is
+//      exact when x is near the mean (Sterbenz), so no cancellation error
+//      is amplified by a large invstd; only the mean's tiny low part goes
+//      into the shift (the form x·scale + (β − mean·scale) would lose that
+//      protection).
 // Traffic: x is read twice and y written once (2+2+2 bytes per bf16 element).
+// The statistics kernels read x through the coherent path with the default
+// L2 policy and the apply walks replicas and vectors in the reverse order,
+// so the apply's second read of x finds the part of x still in L2 (all of
+// it when x is smaller than L2) before the part that has left it.
 #include <cstdint>
 #include <map>
 #include <mutex>
@@ -90,6 +96,7 @@ struct BnParams {
     float eps;
     float inv_hi, inv_lo;  // 1 / (n * batch * H * W) as a float pair
     int32_t tree_top;      // merge: first shuffle offset (lanes >= min(S, 32) hold no sums)
+    FastDiv div_vs8;       // apply mode 3: 8-element vectors per sample (C*H*W/8)
 };
 
 template <bool BF16>
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
             const uint64_t src = a0al + 16ull * v;
             unsigned char* dst = stage + j * a.slot_bytes + 16 * v;
             if (src < a1fl) {
-                *reinterpret_cast<uint4*>(dst) = ld16<true>(base + src);
+                *reinterpret_cast<uint4*>(dst) = ld16_keep(base + src);
             } else if (src < a1) {                      // ragged end, element by element
                 const uint64_t lo = src > a0 ? src : a0;
                 const uint64_t hi = (src + 16 < a1) ? src + 16 : a1;
@@ -546,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 5) bn_stats_plane_kernel(const __gri
             for (int u = 0; u < 2; ++u) {
                 const uint32_t v = cc * kChunkVecs + u * 32 + lane;
                 ok[i][u] = ch < total && v < units;
-                raw[i][u] = ok[i][u] ? ld16<true>(base + static_cast<int64_t>(v) * 16) : make_uint4(0, 0, 0, 0);
+                raw[i][u] = ok[i][u] ? ld16_keep(base + static_cast<int64_t>(v) * 16) : make_uint4(0, 0, 0, 0);
             }
         }
 #pragma unroll
@@ -699,10 +706,16 @@ __device__ __forceinline__ uint32_t channel_of(uint32_t e, const BnParams& a) {
 
 // CMODE: 0 = H*W a multiple of 8 (one channel per 8-element vector);
 //        1 = H*W >= 8 (at most one channel boundary inside a vector);
-//        2 = H*W < 8 (channel per element).
+//        2 = H*W < 8 (channel per element);
+//        3 = as 1, with the grid stride a whole number of samples: every
+//            vector a thread visits sits at the same position of its
+//            sample, so the thread finds its channels and packs their
+//            coefficients once, before its loop.
 template <bool BF16_IN, bool BF16_OUT, int CMODE, bool NC>
 __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constant__ BnParams a) {
-    const int r = blockIdx.y;
+    // replicas and vectors are visited in the reverse of the statistics pass's order (its last CTAs
+    // read the last samples), so the x still in L2 from that pass is read first
+    const int r = gridDim.y - 1 - blockIdx.y;
     const char* x = static_cast<const char*>(a.x[r]);
     char* y = static_cast<char*>(a.y[r]);
     constexpr int ISZ = BF16_IN ? 2 : 4, OSZ = BF16_OUT ? 2 : 4;
@@ -717,8 +730,9 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
         for (int u = 0; u < 4; ++u) {
             const uint32_t v = v0 + u * stride;
             if (v < nvec) {
-                raw[u][0] = ld16<NC>(x + static_cast<int64_t>(v) * 8 * ISZ);
-                if constexpr (!BF16_IN) raw[u][1] = ld16<NC>(x + static_cast<int64_t>(v) * 8 * ISZ + 16);
+                const uint32_t vr = nvec - 1 - v;        // reverse order
+                raw[u][0] = ld16<NC>(x + static_cast<int64_t>(vr) * 8 * ISZ);
+                if constexpr (!BF16_IN) raw[u][1] = ld16<NC>(x + static_cast<int64_t>(vr) * 8 * ISZ + 16);
             }
         }
     };
@@ -727,13 +741,35 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
     // in the stream had completed; the coefficients are read after the wait
     if (gtid < nvec) load4(gtid);
     pdl_enter();
+    // mode 3: the coefficient pairs of this thread's element positions (fixed for all its vectors)
+    uint64_t M2[4], S2[4], T2[4];
+    if constexpr (CMODE == 3) {
+        float4 kA = make_float4(0.0f, 0.0f, 0.0f, 0.0f), kB = kA;
+        uint32_t eb = 8;
+        if (gtid < nvec) {
+            const uint32_t vr = nvec - 1 - gtid;
+            const uint32_t e0 = (vr - fdiv(vr, a.div_vs8) * static_cast<uint32_t>(a.div_vs8.d)) * 8;   // in the sample
+            const uint32_t cA = fdiv(e0, a.div_hw);
+            eb = (cA + 1) * static_cast<uint32_t>(a.HW) - e0;
+            kA = __ldg(a.coef + cA);
+            kB = eb < 8 ? __ldg(a.coef + cA + 1) : kA;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4& lo = static_cast<uint32_t>(2 * j) < eb ? kA : kB;
+            const float4& hi = static_cast<uint32_t>(2 * j + 1) < eb ? kA : kB;
+            M2[j] = f2_pack(lo.x, hi.x);
+            S2[j] = f2_pack(lo.y, hi.y);
+            T2[j] = f2_pack(lo.z, hi.z);
+        }
+    }
     for (uint32_t v0 = gtid; v0 < nvec; v0 += 4 * stride) {
         if (v0 != gtid) load4(v0);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const uint32_t v = v0 + u * stride;
             if (v >= nvec) continue;
-            const uint32_t e0 = v * 8;
+            const uint32_t e0 = (nvec - 1 - v) * 8;
             uint64_t xv[4];                                 // element pairs (2j, 2j + 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
@@ -753,6 +789,9 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
                 for (int j = 0; j < 4; ++j)
                     yv2[j] = normalize2(xv[j], static_cast<uint32_t>(2 * j) < cross ? k0 : k1,
                                         static_cast<uint32_t>(2 * j + 1) < cross ? k0 : k1);
+            } else if constexpr (CMODE == 3) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) yv2[j] = f2_fma(f2_sub(xv[j], M2[j]), S2[j], T2[j]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -981,6 +1020,7 @@ template <bool BF16_IN, bool BF16_OUT>
 int launch_apply(const BnParams& p, int cmode, bool nc, dim3 grid, cudaStream_t s) {
     if (cmode == 0) return launch_apply_mode<BF16_IN, BF16_OUT, 0>(p, nc, grid, s);
     if (cmode == 1) return launch_apply_mode<BF16_IN, BF16_OUT, 1>(p, nc, grid, s);
+    if (cmode == 3) return launch_apply_mode<BF16_IN, BF16_OUT, 3>(p, nc, grid, s);
     return launch_apply_mode<BF16_IN, BF16_OUT, 2>(p, nc, grid, s);
 }
 
@@ -1124,8 +1164,27 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     int64_t cap = (kApplyWaves * resident + n_replicas - 1) / n_replicas;
     if (gx > cap) gx = cap;
     if (gx < 1) gx = 1;
+    int cmode = (p.HW % 8) == 0 ? 0 : (p.HW >= 8 ? 1 : 2);
+    if (cmode == 1 && (static_cast<int64_t>(C) * p.HW) % 8 == 0) {
+        // mode 3: a grid stride (gx*kThreads vectors) that is a whole number of samples, with gx the
+        // multiple of the smallest such count nearest to the size chosen above
+        const int64_t vs8 = static_cast<int64_t>(C) * p.HW / 8;
+        int64_t gcd = kThreads, tmp = vs8;
+        while (tmp != 0) {                                  // gcd(kThreads, vs8)
+            const int64_t q = gcd % tmp;
+            gcd = tmp;
+            tmp = q;
+        }
+        const int64_t m0 = vs8 / gcd;                       // CTAs per whole number of samples
+        int64_t g3 = (gx + m0 / 2) / m0 * m0;
+        if (g3 < m0) g3 = m0;
+        if (g3 <= 2 * gx + m0 && g3 * kThreads <= (int64_t(1) << 31) / 4) {
+            gx = g3;
+            cmode = 3;
+            p.div_vs8 = make_fastdiv(static_cast<uint32_t>(vs8));
+        }
+    }
     const dim3 agrid(static_cast<unsigned>(gx), static_cast<unsigned>(n_replicas));
-    const int cmode = (p.HW % 8) == 0 ? 0 : (p.HW >= 8 ? 1 : 2);
     const bool nc = !in_place_any;
     const bool bf16_out = out_dtype == DDP_BF16;
     if (bf16_in) return bf16_out ? launch_apply<true, true>(p, cmode, nc, agrid, s) : launch_apply<true, false>(p, cmode, nc, agrid, s);

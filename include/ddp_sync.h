@@ -447,7 +447,8 @@ int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtyp
  *   Arguments, results and errors are those of syncbn_merge_apply, without
  *   workspace/workspace_bytes.  Sizes whose syncbn_workspace_bytes(...)
  *   exceeds the fixed array are rejected with DDP_ERR_CAPACITY (every shape
- *   with C <= 43690 fits; C <= 2048 needs at most 544 KiB).
+ *   with C <= 43690 fits: the planner keeps every workspace within 1 MiB
+ *   for those).
  *   Set-up: the first call on each device looks up the array's device
  *   address (cudaGetSymbolAddress, with that device current) and caches it;
  *   make that first call before any stream capture.  The address stays
