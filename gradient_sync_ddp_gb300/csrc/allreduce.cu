@@ -302,11 +302,15 @@ __global__ void __launch_bounds__(kThreads) sgd_kernel(const __grid_constant__ S
 // at least kMultiWaveVecs vectors gets up to kWaves waves instead (each
 // thread still at least kMinVecsPerThread vectors).  Measured on GB300:
 // fused SGD over GPT-2-small buckets 6.58 -> 7.24 TB/s and the bf16 average
-// 6.89 -> 7.19 TB/s with 16 waves, while 25 MiB fp32 buckets (14 vectors per
-// thread at one wave) ran 3 % slower with several.
+// 6.89 -> 7.19 TB/s with 16 waves (8 vectors per thread at least).  With the
+// thresholds lowered to 8 and 2, the 25 MiB fp32 buckets (14 vectors per
+// thread at one wave) also run several waves of short CTAs: the ResNet-50
+// step 7.08 -> 7.13 TB/s (one launch alone 27.62 -> 27.35 us), SGD 7.35 ->
+// 7.39, the bf16 average 7.23 -> 7.33, ring / tree order 6.87 / 6.87 -> 6.94
+// / 7.06 TB/s; thresholds 8 and 1 were within noise of these.
 constexpr int kWaves = 16;
-constexpr int64_t kMultiWaveVecs = 32;
-constexpr int64_t kMinVecsPerThread = 8;
+constexpr int64_t kMultiWaveVecs = 8;
+constexpr int64_t kMinVecsPerThread = 2;
 
 template <typename Params>
 int launch_wave(void (*kernel)(Params), int64_t nvec, cudaStream_t s, const Params& p, int max_grid = 1 << 30) {

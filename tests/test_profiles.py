@@ -9,7 +9,7 @@ import re
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PROFILES = os.path.join(ROOT, "profiles")
 CSRC = os.path.join(ROOT, "gradient_sync_ddp_gb300", "csrc")
-LINE = re.compile(r"source_sha256:\s*([0-9a-f]{16})(?:\s+over\s+(.+))?")
+LINE = re.compile(r"source_sha256:\s*([0-9a-f]{16})(?:\s+over\s+([\w.]+(?:,\s*[\w.]+)*))?")
 
 
 def _summaries():
