@@ -61,7 +61,7 @@ typedef enum {
     DDP_ERR_ALIGNMENT = -2,     /* a device pointer is not 16-byte aligned */
     DDP_ERR_CAPACITY = -3,      /* an output array or workspace is too small */
     DDP_ERR_CUDA = -4,          /* a CUDA call failed; see ddp_last_cuda_error() */
-    DDP_ERR_UNSUPPORTED = -5,   /* valid request this build does not implement */
+    DDP_ERR_UNSUPPORTED = -5,   /* valid request the library does not implement */
     DDP_ERR_TIMEOUT = -6        /* a bounded wait or loop ran out (see each entry) */
 } ddp_status;
 

@@ -34,7 +34,7 @@ def test_headline_is_short_and_complete():
                 "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e",
                 "gpu_launches", "clocks"):
         assert key in line, key
-    assert line["metric"] == json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"]
+    assert line["metric"] == bench.METRIC
     assert "workload" in line["config"]
     for key in ("bound", "achieved", "peak", "unit", "frac", "traffic"):
         assert key in line["roofline"], key
