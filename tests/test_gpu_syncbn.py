@@ -84,7 +84,8 @@ def _run(g, xs_dev, ys_dev, C, eps=1e-5, gamma=None, beta=None):
                                    (1, 1, 3, 111, 111), (2, 3, 5, 64, 64), (8, 32, 2048, 7, 7),
                                    (2, 2, 70, 3, 7), (2, 2, 300, 1, 5), (3, 2, 260, 1, 7),
                                    (2, 3, 4, 67, 8), (5, 3, 24, 7, 7), (2, 3, 12, 14, 14), (6, 5, 32, 5, 5),
-                                   (3, 7, 40, 28, 28), (16, 2, 8, 56, 56), (2, 2, 40000, 2, 4)])
+                                   (3, 7, 40, 28, 28), (16, 2, 8, 56, 56), (2, 2, 40000, 2, 4),
+                                   (2, 2, 512, 14, 14), (2, 1, 2048, 7, 7)])
 @pytest.mark.parametrize("io", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "f32"), ("f32", "bf16")])
 def test_small_shapes(g, shape, io):
     n, B, C, H, W = shape
