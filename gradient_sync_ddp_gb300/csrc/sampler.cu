@@ -83,17 +83,22 @@ __device__ __forceinline__ uint32_t round_fn(uint32_t x, int i, const SamplerPar
     return h ^ __umulhi(h, a.sh16);
 }
 
-// One pass of the network on x = (H, L), H the high ceil(bits/2) bits and L
-// the low floor(bits/2) bits: even rounds H ^= fmix32(L ^ k_i) mod 2^|H|,
-// odd rounds L ^= fmix32(H ^ k_i) mod 2^|L|.  Every round undoes itself, so
-// the pass is a bijection.
-template <bool NARROW>
-__device__ __forceinline__ void encrypt(uint32_t& H, uint32_t& L, const SamplerParams& a) {
-#pragma unroll
-    for (int i = 0; i < kRounds; ++i) {
-        if (i % 2 == 0) H ^= round_fn<NARROW>(L, i, a) & a.mask_hi;
-        else L ^= round_fn<NARROW>(H, i, a) & a.mask_lo;
-    }
+// One pass of the network on x = H * 2^h_lo + L, H the high ceil(bits/2)
+// bits and L the low floor(bits/2) bits: even rounds H ^= fmix32(L ^ k_i)
+// mod 2^|H|, odd rounds L ^= fmix32(H ^ k_i) mod 2^|L|.  Every round undoes
+// itself, so the pass is a bijection.  The halves are carried as 32-bit words
+// whose bits above the half's width are don't-cares: a round's output is
+// xored in unmasked, and the mask is applied where the half is read (fused
+// with the key xor), which is the same arithmetic mod 2^|half|.
+template <bool NARROW, typename U>
+__device__ __forceinline__ U encrypt(U x, const SamplerParams& a) {
+    uint32_t L = static_cast<uint32_t>(x);                  // bits above h_lo: don't-care
+    uint32_t H = static_cast<uint32_t>(x >> a.h_lo);        // exact: x < 2^bits
+    H ^= round_fn<NARROW>(L & a.mask_lo, 0, a);
+    L ^= round_fn<NARROW>(H & a.mask_hi, 1, a);
+    H ^= round_fn<NARROW>(L & a.mask_lo, 2, a);
+    L ^= round_fn<NARROW>(H & a.mask_hi, 3, a);
+    return static_cast<U>(H & a.mask_hi) * a.p2lo + (L & a.mask_lo);
 }
 
 // Padded-list position -> unshuffled index: padding repeats the head.
@@ -103,21 +108,64 @@ __device__ __forceinline__ U wrap(U pos, U n) {
     return pos - n < n ? pos - n : pos % n;    // pos >= 2n only when N > n
 }
 
-// A pool is per_warp consecutive slots s0 .. s0+len-1 of one rank's row r;
-// slot s holds padded-list position r + s*N.  Warps take pools grid-stride;
-// the host sizes pools so that the grid is kBlocksPerSm CTAs on every SM.
-// Cycle-walk lengths are geometric: instead of idling until the slowest
-// lane of the warp has finished, a lane whose walk ends writes its index and
-// takes the pool's next unclaimed slot (ballot + prefix count), so every
-// iteration is one encryption per lane until the pool runs dry.  The body
-// uses selects, not branches; a lane without a slot computes on a clamped
-// copy and stores nothing.  U is uint32_t when n <= 2^31: then every
+// Unshuffled index of slot s of a pool whose first slot is position pos0.
+// PAD: the pool holds padded positions (>= n); otherwise no wrap is needed.
+template <typename U, bool PAD>
+__device__ __forceinline__ U slot_index(U pos0, int32_t s, U N, U n) {
+    const U pos = pos0 + static_cast<U>(s) * N;
+    return PAD ? wrap<U>(pos, n) : pos;
+}
+
+// The walks of one pool: per_warp consecutive slots 0 .. len-1 of one rank's
+// row, slot s holding padded-list position pos0 + s*N.  Cycle-walk lengths
+// are geometric: instead of idling until the slowest lane of the warp has
+// finished, a lane whose walk ends writes its index and takes the pool's
+// next unclaimed slot (ballot + prefix count), so every iteration is one
+// encryption per lane until the pool runs dry.  The body uses selects, not
+// branches; a lane without a slot walks a copy of the last slot and stores
+// nothing.  The walk bound can only be reached once the loop has run
+// kWalkCap times, so its check sits behind that warp-uniform test.
+template <typename U, bool PAD>
+__device__ __forceinline__ void walk_pool(const SamplerParams& a, int64_t* out, U pos0, int32_t len, int lane) {
+    constexpr bool kNarrow = sizeof(U) == 4;
+    const unsigned lanes_below = (1u << lane) - 1u;
+    const U n = static_cast<U>(a.n), N = static_cast<U>(a.N);
+    const int32_t last = len - 1;
+    int32_t off = lane;                           // this lane's slot in the pool
+    U x = slot_index<U, PAD>(pos0, min(off, last), N, n);
+    int32_t deadline = kWalkCap;                  // loop count at which this lane's walk gives up
+    int32_t next = 32;                            // first unclaimed slot of the pool
+    for (int32_t it = 1;; ++it) {
+        const bool live = off < len;
+        if (!__any_sync(0xffffffffu, live)) break;
+        x = encrypt<kNarrow>(x, a);
+        const bool hit = x < n;
+        if (live && hit) out[off] = static_cast<int64_t>(x);
+        bool done = hit;
+        if (it >= kWalkCap) {                     // warp-uniform; never reached in practice
+            const bool give_up = !hit && it >= deadline;
+            if (live && give_up) {
+                out[off] = -1;
+                if (a.status) atomicAdd(a.status, 1);
+            }
+            done = done || give_up;
+        }
+        const unsigned fin = __ballot_sync(0xffffffffu, done);
+        const int32_t o = next + __popc(fin & lanes_below);
+        next += __popc(fin);
+        const U xn = slot_index<U, PAD>(pos0, min(o, last), N, n);
+        off = done ? o : off;
+        x = done ? xn : x;
+        deadline = done ? it + kWalkCap : deadline;
+    }
+}
+
+// Warps take pools grid-stride; the host sizes pools so that the grid is
+// kBlocksPerSm CTAs on every SM.  U is uint32_t when n <= 2^31: then every
 // position is below total < n + N < 2^32 and both halves below 2^16.
 template <typename U>
 __global__ void __launch_bounds__(kSamplerThreads) sampler_kernel(const __grid_constant__ SamplerParams a) {
-    constexpr bool kNarrow = sizeof(U) == 4;
     const int lane = threadIdx.x & 31;
-    const unsigned lanes_below = (1u << lane) - 1u;
     const U n = static_cast<U>(a.n);
     const U N = static_cast<U>(a.N);
     const int64_t warps = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
@@ -133,33 +181,8 @@ __global__ void __launch_bounds__(kSamplerThreads) sampler_kernel(const __grid_c
             for (int32_t o = lane; o < len; o += 32) out[o] = static_cast<int64_t>(wrap<U>(pos0 + o * N, n));
             continue;
         }
-        int32_t off = lane;                        // this lane's slot in the pool
-        U b = wrap<U>(pos0 + static_cast<U>(min(off, len - 1)) * N, n);
-        uint32_t H = static_cast<uint32_t>(b >> a.h_lo), L = static_cast<uint32_t>(b) & a.mask_lo;
-        int32_t steps = 0;                         // encryptions since the walk began
-        int32_t next = 32;                         // first unclaimed slot of the pool
-        while (__any_sync(0xffffffffu, off < len)) {
-            encrypt<kNarrow>(H, L, a);
-            const U y = static_cast<U>(H) * a.p2lo + L;
-            ++steps;
-            const bool live = off < len;
-            const bool hit = y < n;
-            if (live && hit) out[off] = static_cast<int64_t>(y);
-            const bool done = live && (hit || steps >= kWalkCap);
-            if (done && !hit) {                    // walk bound reached: never observed
-                out[off] = -1;
-                if (a.status) atomicAdd(a.status, 1);
-            }
-            const unsigned fin = __ballot_sync(0xffffffffu, done);
-            const int32_t o = next + __popc(fin & lanes_below);
-            next += __popc(fin);
-            b = wrap<U>(pos0 + static_cast<U>(min(o, len - 1)) * N, n);
-            const uint32_t Hn = static_cast<uint32_t>(b >> a.h_lo), Ln = static_cast<uint32_t>(b) & a.mask_lo;
-            off = done ? o : off;
-            H = done ? Hn : H;
-            L = done ? Ln : L;
-            steps = done ? 0 : steps;
-        }
+        if (pos0 + static_cast<U>(len - 1) * N >= n) walk_pool<U, true>(a, out, pos0, len, lane);
+        else walk_pool<U, false>(a, out, pos0, len, lane);
     }
 }
 
