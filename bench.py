@@ -803,9 +803,11 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None, rows_out=None):
             ms = _time_launches(torch, lambda: [g.syncbn_merge_apply(*sets[i % R], mean, inv, ws)
                                                 for i in range(SYNCBN_CALLS)], 10, side) / SYNCBN_CALLS
             nbytes = 6 * N_REPLICAS * B * C * H * W
+            parts = g.syncbn_channel_parts(N_REPLICAS, g.BF16, B, C, H, W)
             emit_row(f"syncbn_{C}x{H}x{W}", {"workload": f"SyncBN 8 x [32,{C},{H},{W}] bf16", "ms": ms, "bytes": nbytes,
                                            "GBps": nbytes / ms / 1e6, "frac": nbytes / ms / 1e6 / peak,
-                                           "launches": 3, "calls_per_graph": SYNCBN_CALLS, "input_sets": R,
+                                           "launches": 3 * parts, "streams": parts,
+                                           "calls_per_graph": SYNCBN_CALLS, "input_sets": R,
                                            "l2": f"{R} input sets rotated: {R * 2 * xbytes / 1e6:.0f} MB of x and y "
                                                  f"against {L2_BYTES / 1e6:.0f} MB of L2"}, rows_out)
             del sets

@@ -57,6 +57,8 @@ _lib.ddp_bucket_allreduce_sgd.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int64
 _lib.ddp_bucket_allreduce_sgd.restype = _c.c_int
 _lib.syncbn_workspace_bytes.argtypes = [_c.c_int32] * 5
 _lib.syncbn_workspace_bytes.restype = _c.c_size_t
+_lib.syncbn_channel_parts.argtypes = [_c.c_int32] * 6
+_lib.syncbn_channel_parts.restype = _c.c_int
 _lib.syncbn_merge_apply.argtypes = [_P, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
                                     _c.c_float, _P, _P, _P, _c.c_int32, _P, _P, _P, _c.c_size_t, _P]
 _lib.syncbn_merge_apply.restype = _c.c_int
@@ -197,6 +199,15 @@ def ddp_bucket_allreduce_sgd(replicas, param, momentum_buf, lr: float, momentum:
 
 def syncbn_workspace_bytes(n_replicas: int, batch: int, C: int, H: int, W: int) -> int:
     return int(_lib.syncbn_workspace_bytes(n_replicas, batch, C, H, W))
+
+
+def syncbn_channel_parts(n_replicas: int, in_dtype: int, batch: int, C: int, H: int, W: int) -> int:
+    """2 when syncbn_merge_apply runs these sizes as two channel halves on
+    two streams, 1 for one sequence on the caller's stream (in_dtype: F32 or
+    BF16)."""
+    r = int(_lib.syncbn_channel_parts(n_replicas, in_dtype, batch, C, H, W))
+    _check(r if r < 0 else 0, "syncbn_channel_parts")
+    return r
 
 
 def syncbn_merge_apply(xs, ys, mean_out, invstd_out, workspace, eps: float = 1e-5, gamma=None, beta=None,

@@ -6,19 +6,23 @@
 // AI_Infra notes "1.DataParallel / DDP" §4.3: the synced statistics are those
 // of the whole global batch (one extra all-reduce per BN layer).
 //
-// Three launches on the caller's stream:
+// Three launches on the caller's stream (large aligned-plane calls: three for
+// each channel half, the second half on a side stream joined back before the
+// call returns):
 //   1. stats  — per-channel partial sums over slices of the N*batch samples.
 //      The sums are shifted by K_c, the channel's first element (replica 0,
 //      sample 0): d = x − K_c, and Σd, Σd² are accumulated, so Q/M − mean²
 //      never subtracts two large nearly equal numbers when |mean| >> std.
 //      The kernel depends on the plane (H*W contiguous elements of one
 //      sample and channel):
-//        plane kernel — H*W a multiple of the 16-byte vector (56x56, 28x28):
+//        plane kernel — H*W a multiple of the 16-byte vector and at least
+//          64 vectors long (56x56, 28x28):
 //          CTA (c, s) streams its planes with 16-byte loads, a warp at a
 //          time over 64-vector chunks of one plane, two element positions
 //          per packed f32x2 instruction.
 //        bulk-staged kernel — unaligned planes at least one vector long
-//          (7x7, 14x14, 3x3): a CTA owns G consecutive channels (G*H*W about
+//          (7x7, 14x14, 3x3) and aligned bf16 ones under 16 vectors (8x8, 4x4):
+//          a CTA owns G consecutive channels (G*H*W about
 //          2K elements) and a slice of the samples; for one sample those G
 //          channels are one contiguous run, copied into shared memory by one
 //          bulk asynchronous copy, and each lane sums a contiguous range of
@@ -69,6 +73,7 @@ constexpr int64_t kMaxPartials = 65536;  // C*S bound: fp32 partials stay <= 512
 constexpr int kRunElems = 2048;          // channels per group: G*H*W <= this (G >= 1)
 constexpr int kStageBytes = 32768;       // shared staging buffer per CTA (staged group kernel)
 constexpr int kPlaneVecsPerThread = 24;  // plane statistics: slices sized for this many vectors per thread
+constexpr int kPlaneMinVecs = 16;        // aligned bf16 planes of fewer vectors: bulk-staged statistics
 constexpr int kApplyWaves = 16;          // apply grid: at most this many waves of 8 CTAs per SM
 constexpr int kApplyVecs = 8;            // apply grid: at least this many 16-byte vectors per thread
 
@@ -91,12 +96,20 @@ struct BnParams {
     int32_t G;          // group kernel: channels per CTA (power of two)
     int32_t R;          // group kernel: runs staged per tile
     int32_t slot_bytes; // group kernel: shared bytes per staged run
-    int32_t tc_log2;    // bulk kernel: log2 of the lanes per channel (32/G for G < 32, else 0)
+    int32_t tc_log2;    // bulk kernel: log2 of the lanes per channel (see plan_stats)
+    int32_t vec_reads;  // bulk kernel: every lane's range starts 16-byte aligned (16-byte shared reads)
     uint64_t buf_fl;    // bulk kernel: replica bytes rounded down to 16 (copies stop there)
     float eps;
     float inv_hi, inv_lo;  // 1 / (n * batch * H * W) as a float pair
     int32_t tree_top;      // merge: first shuffle offset (lanes >= min(S, 32) hold no sums)
     FastDiv div_vs8;       // apply mode 3: 8-element vectors per sample (C*H*W/8)
+    // channel range of this launch sequence: [0, C) for a whole call, half of it for each of
+    // the two channel halves a call may run concurrently (plane statistics, apply mode 0)
+    int32_t c_base, c_end;
+    int32_t parted;        // 1: [c_base, c_end) is a strict part of [0, C)
+    FastDiv div_vp;        // parted apply: 8-element vectors of one sample within the part
+    uint32_t vs_full;      // parted apply: 8-element vectors per sample (C*H*W/8)
+    uint32_t v_base;       // parted apply: the part's first vector within a sample (c_base*H*W/8)
 };
 
 template <bool BF16>
@@ -250,7 +263,8 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
 }
 
 // Bulk-staged kernel, grid (ceil(C/G), S), for H*W >= the vector width W
-// and not a multiple of it (7x7, 14x14, 3x3, ...).  A run (one sample's G
+// and not a multiple of it (7x7, 14x14, 3x3, ...), or (bf16) a multiple of
+// it shorter than 16 vectors (8x8, 4x4).  A run (one sample's G
 // consecutive channels) is contiguous in memory; the 16-byte aligned blocks
 // that cover it are copied into shared memory by one bulk asynchronous copy
 // (the copy engine moves them without registers; completion is counted on
@@ -301,7 +315,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // of the shared buffer `buf` (element aligned; 32-bit words read).
 template <bool BF16>
 __device__ __forceinline__ void sum_range(const unsigned char* buf, uint32_t byte0, uint32_t count, float K,
-                                          float& acc_s, float& acc_q) {
+                                          bool vec_reads, float& acc_s, float& acc_q) {
     // element pairs in packed f32x2 accumulators, a ragged first or last element in scalar ones
     float s0 = 0.0f, q0 = 0.0f;
     const uint64_t K2 = f2_pack(K, K);
@@ -320,6 +334,15 @@ __device__ __forceinline__ void sum_range(const unsigned char* buf, uint32_t byt
             s0 += d;
             q0 = fmaf(d, d, q0);
             ++h;
+        }
+        if (vec_reads) {                                     // every lane's range 16-byte aligned
+            for (; h + 8 <= hend; h += 8) {
+                const uint4 q = *reinterpret_cast<const uint4*>(w + (h >> 1));
+                add_pair(bf16_lo(q.x), bf16_hi(q.x));
+                add_pair(bf16_lo(q.y), bf16_hi(q.y));
+                add_pair(bf16_lo(q.z), bf16_hi(q.z));
+                add_pair(bf16_lo(q.w), bf16_hi(q.w));
+            }
         }
         for (; h + 8 <= hend; h += 8) {
             uint32_t v[4];
@@ -373,8 +396,8 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     const int ntiles = (p1 - p0 + R - 1) / R;
     const uint32_t buf_bytes = static_cast<uint32_t>(R) * a.slot_bytes;
     const uint32_t run_bytes = static_cast<uint32_t>(Gc) * HW * ESZ;
-    // this lane's channels (CPL = G/32 of them when G >= 32) and element range within a plane;
-    // Tc = 2^tc_log2 lanes per channel (G < 32), so the splits are shifts
+    // this lane's CPL channels (lane/Tc, then every 32/Tc-th) and its element range, part
+    // lane%Tc of Tc = 2^tc_log2 equal parts of a plane (the splits are shifts)
     const int Tc = 1 << a.tc_log2;
     const int part = lane & (Tc - 1);
     const uint32_t e_lo = (static_cast<uint32_t>(HW) * part) >> a.tc_log2;
@@ -384,7 +407,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     pdl_wait_then_release();   // must stay the wait-then-release form: the apply reads x before its own wait
 #pragma unroll
     for (int m = 0; m < CPL; ++m) {
-        cl[m] = a.G >= 32 ? lane + 32 * m : lane >> a.tc_log2;
+        cl[m] = (lane >> a.tc_log2) + (32 >> a.tc_log2) * m;
         K[m] = cl[m] < Gc ? load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + cl[m]) * HW) : 0.0f;
         acc_s[m] = 0.0f;
         acc_q[m] = 0.0f;
@@ -471,7 +494,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
             for (int m = 0; m < CPL; ++m) {
                 if (cl[m] < Gc)
                     sum_range<BF16>(run, pre + (static_cast<uint32_t>(cl[m]) * HW + e_lo) * ESZ, e_hi - e_lo, K[m],
-                                    acc_s[m], acc_q[m]);
+                                    a.vec_reads != 0, acc_s[m], acc_q[m]);
             }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // reads done before the next bulk writes
@@ -491,9 +514,10 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     __syncthreads();
     if (threadIdx.x < Gc) {
         const int c = threadIdx.x;
-        const int m = a.G >= 32 ? c / 32 : 0;
-        const int l0 = a.G >= 32 ? c % 32 : c * Tc;
-        const int nl = a.G >= 32 ? 1 : Tc;
+        const int cps = 32 >> a.tc_log2;          // channels per 32 lanes
+        const int m = c / cps;
+        const int l0 = (c % cps) << a.tc_log2;
+        const int nl = Tc;
         FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
         for (int w = 0; w < kWarps; ++w)
             for (int l = l0; l < l0 + nl; ++l) {
@@ -519,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 5) bn_stats_plane_kernel(const __gri
     constexpr int W = BF16 ? 8 : 4;    // elements per 16-byte access
     constexpr int ESZ = BF16 ? 2 : 4;
     constexpr int kWarps = kThreads / 32;
-    const int c = blockIdx.x, s = blockIdx.y;
+    const int c = a.c_base + blockIdx.x, s = blockIdx.y;
     const int lane = threadIdx.x % 32, warp = threadIdx.x / 32;
     int p0, p1;
     slice_bounds(a, s, p0, p1);
@@ -639,18 +663,18 @@ template <bool BF16>
 __global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_constant__ BnParams a) {
     __shared__ FF sums[2][32];
     const int w = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int c = blockIdx.x * 32 + w;
-    const int cc = blockIdx.x * 32 + lane;   // warp 0: the channel this lane finalises
+    const int c = a.c_base + blockIdx.x * 32 + w;
+    const int cc = a.c_base + blockIdx.x * 32 + lane;   // warp 0: the channel this lane finalises
     pdl_enter();
     // warp 0 fetches its channels' shift K, gamma and beta while the partials are summed
     float Kc = 0.0f, gc = 1.0f, bc = 0.0f;
-    if (w == 0 && cc < a.C) {
+    if (w == 0 && cc < a.c_end) {
         Kc = load_elem<BF16>(a.x[0], static_cast<int64_t>(cc) * a.HW);
         if (a.gamma) gc = a.gamma[cc];
         if (a.beta) bc = a.beta[cc];
     }
     FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
-    if (c < a.C) {
+    if (c < a.c_end) {
         const float2* p = a.partial + static_cast<int64_t>(c) * a.S;
         int s0 = lane;
         for (; s0 + 96 < a.S; s0 += 128) {           // four independent loads in flight
@@ -673,7 +697,7 @@ __global__ void __launch_bounds__(kMergeThreads) bn_merge_kernel(const __grid_co
         sums[1][w] = Q;
     }
     __syncthreads();
-    if (w != 0 || cc >= a.C) return;
+    if (w != 0 || cc >= a.c_end) return;
     const FF inv{a.inv_hi, a.inv_lo};            // 1/M as a float pair
     const FF ms = ff_mul(sums[0][lane], inv);    // mean of the shifted values
     const FF mean = ff_add(FF{Kc, 0.0f}, ms);
@@ -710,7 +734,9 @@ __device__ __forceinline__ uint32_t channel_of(uint32_t e, const BnParams& a) {
 //        3 = as 1, with the grid stride a whole number of samples: every
 //            vector a thread visits sits at the same position of its
 //            sample, so the thread finds its channels and packs their
-//            coefficients once, before its loop.
+//            coefficients once, before its loop;
+//        4 = as 0, over the channels [c_base, c_end) only: the launch's
+//            vectors are those channels' runs in each sample.
 template <bool BF16_IN, bool BF16_OUT, int CMODE, bool NC>
 __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constant__ BnParams a) {
     // replicas and vectors are visited in the reverse of the statistics pass's order (its last CTAs
@@ -719,10 +745,18 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
     const char* x = static_cast<const char*>(a.x[r]);
     char* y = static_cast<char*>(a.y[r]);
     constexpr int ISZ = BF16_IN ? 2 : 4, OSZ = BF16_OUT ? 2 : 4;
-    const uint32_t E = static_cast<uint32_t>(a.batch) * a.C * a.HW;
+    const uint32_t E = static_cast<uint32_t>(a.batch) * (a.c_end - a.c_base) * a.HW;   // this launch's elements
     const uint32_t nvec = E / 8;
     const uint32_t stride = gridDim.x * kThreads;
     const uint32_t gtid = blockIdx.x * kThreads + threadIdx.x;
+    // vector index within the replica of this launch's vector vr (mode 4: a part of the channels)
+    auto full_vec = [&](uint32_t vr) -> uint32_t {
+        if constexpr (CMODE == 4) {
+            const uint32_t b = fdiv(vr, a.div_vp);
+            return b * a.vs_full + a.v_base + (vr - b * static_cast<uint32_t>(a.div_vp.d));
+        }
+        return vr;
+    };
     // the loads of 4 vectors, issued before any arithmetic
     uint4 raw[4][2];
     auto load4 = [&](uint32_t v0) {
@@ -730,7 +764,7 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
         for (int u = 0; u < 4; ++u) {
             const uint32_t v = v0 + u * stride;
             if (v < nvec) {
-                const uint32_t vr = nvec - 1 - v;        // reverse order
+                const uint32_t vr = full_vec(nvec - 1 - v);   // reverse order
                 raw[u][0] = ld16<NC>(x + static_cast<int64_t>(vr) * 8 * ISZ);
                 if constexpr (!BF16_IN) raw[u][1] = ld16<NC>(x + static_cast<int64_t>(vr) * 8 * ISZ + 16);
             }
@@ -769,13 +803,13 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
         for (int u = 0; u < 4; ++u) {
             const uint32_t v = v0 + u * stride;
             if (v >= nvec) continue;
-            const uint32_t e0 = (nvec - 1 - v) * 8;
+            const uint32_t e0 = full_vec(nvec - 1 - v) * 8;
             uint64_t xv[4];                                 // element pairs (2j, 2j + 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 xv[j] = BF16_IN ? vec_pair<true>(raw[u][0], j) : vec_pair<false>(raw[u][j >> 1], j & 1);
             uint64_t yv2[4];
-            if constexpr (CMODE == 0) {
+            if constexpr (CMODE == 0 || CMODE == 4) {
                 const float4 k4 = __ldg(a.coef + channel_of(e0, a));
 #pragma unroll
                 for (int j = 0; j < 4; ++j) yv2[j] = normalize2(xv[j], k4, k4);
@@ -859,8 +893,8 @@ int launch_pdl_smem(void (*kernel)(BnParams), dim3 grid, int smem, cudaStream_t 
 
 // Channels per lane of the bulk-staged kernel: G/32 for G >= 32 (G <= 256).
 template <bool BF16>
-int launch_bulk(int G, dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
-    switch (G >= 32 ? G / 32 : 1) {
+int launch_bulk(int cpl, dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
+    switch (cpl) {
         case 1: return launch_pdl_smem(bn_stats_bulk_kernel<BF16, 1>, grid, smem, s, p);
         case 2: return launch_pdl_smem(bn_stats_bulk_kernel<BF16, 2>, grid, smem, s, p);
         case 4: return launch_pdl_smem(bn_stats_bulk_kernel<BF16, 4>, grid, smem, s, p);
@@ -874,6 +908,8 @@ struct StatsPlan {
     StatsKind kind;
     int G, S, R, slot_bytes;
     int smem;           // bulk kernel: dynamic shared bytes (two tile buffers)
+    int tc_log2, cpl;   // bulk kernel: log2 of the lanes per channel, channels per lane
+    bool vec_reads;     // bulk kernel: every lane's range starts on a 16-byte boundary of its run
 };
 
 // Slices of the bulk kernel: about one resident wave of CTAs, so that each
@@ -882,9 +918,12 @@ struct StatsPlan {
 // correctness) depends on it.
 constexpr int kWaveSms = 152;
 
-int bulk_slices(int n_groups, int P, int C, int smem) {
+int bulk_slices(int n_groups, int P, int C, int smem, int cpl) {
     int per_sm = (227 * 1024) / (smem + 1024);              // shared memory per SM, 1 KiB reserved per CTA
-    if (per_sm > 6) per_sm = 6;                             // registers: 6 CTAs of 256 threads
+    // registers: 6 CTAs of 256 threads with one channel per lane (40 registers), 5 with two (48),
+    // 4 with four or eight (59-64)
+    const int reg_cap = cpl >= 4 ? 4 : (cpl == 2 ? 5 : 6);
+    if (per_sm > reg_cap) per_sm = reg_cap;
     if (per_sm < 1) per_sm = 1;
     int64_t S = static_cast<int64_t>(kWaveSms) * per_sm / n_groups;
     if (S > P) S = P;
@@ -922,10 +961,19 @@ int slot_bytes_for(int G, int HW, int esz) {
     return static_cast<int>((static_cast<int64_t>(G) * HW * esz + 14 + 15) / 16 * 16);
 }
 
-// Aligned planes: plane kernel with 16-byte loads.  Unaligned planes at
-// least one vector long: bulk-staged kernel.  Planes shorter than a vector:
-// staged group kernel.  Unaligned planes too long to fit a group's run in
-// the shared buffer: plane kernel with element loads.
+// Aligned planes of at least kPlaneMinVecs vectors: plane kernel with
+// 16-byte loads.  A warp reads 64-vector chunks of one plane, so shorter
+// planes leave lanes idle; measured on 8 x [32, C, H, W] bf16 with about
+// 67 MB of input, plane kernel against bulk-staged kernel (us per call):
+// 4x4 203 / 46, 4x8 113 / 46, 8x8 70 / 47, 8x16 47 / 48, 16x16 36 / 52,
+// 16x24 30 / 36.  Shorter aligned bf16 planes and unaligned planes at
+// least one vector long: bulk-staged kernel (runs of G channels).
+// Short aligned fp32 planes stay with the plane kernel: there a lane adds
+// fewer fp32 values per accumulator (the bulk kernel adds a lane's whole
+// plane into one pair, and on fp32 2x4 planes its means were off by up to
+// 1.5e-7 standard deviations; bf16 differences add exactly).  Planes
+// shorter than a vector: staged group kernel.  Unaligned planes too long to
+// fit a group's run in the shared buffer: plane kernel with element loads.
 StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
     StatsPlan sp{};
     const int P = n * batch;
@@ -933,17 +981,34 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
     const int G = group_channels(C, HW);
     const int slot = slot_bytes_for(G, HW, esz);
     const bool fits = slot <= kStageBytes;
-    if (HW % W == 0) sp.kind = kPlaneVec;
+    if (HW % W == 0 && (HW / W >= kPlaneMinVecs || esz == 4 || !fits)) sp.kind = kPlaneVec;
     else if (!fits) sp.kind = kPlaneScalar;
     else sp.kind = HW >= W ? kBulk : kStaged;
     if (sp.kind == kBulk) {
         sp.G = G;
         sp.slot_bytes = slot;
         sp.R = kBulkBufMax / slot < kBulkRuns ? kBulkBufMax / slot : kBulkRuns;
-        const int cpl = G >= 32 ? G / 32 : 1;
-        const int red = kThreads * cpl * 2 * static_cast<int>(sizeof(float));
+        // lanes per channel: 32/G for G < 32 (each a contiguous part of the plane), else one; on
+        // short aligned planes, up to one 16-byte vector per lane where the plane's vector count
+        // allows (at most 8 channels per lane), so that eight lanes read 128 contiguous bytes of
+        // shared memory: with a lane per channel, every lane of a warp read the same bank on
+        // 128-byte planes (8x8 bf16: 85 us per call against 47)
+        int tl = 0;
+        while ((G << tl) < 32) ++tl;
+        if (HW % W == 0) {
+            const int vp = HW / W;
+            int t = 0;
+            while (t < 5 && vp % (2 << t) == 0 && (G << (t + 1)) <= 32 * 8) ++t;
+            if (t > tl) tl = t;
+        }
+        sp.tc_log2 = tl;
+        sp.cpl = (G << tl) / 32;
+        // aligned runs and parts of whole 16-byte vectors: warp-uniform, so no lane takes the
+        // other loop (on 7x7 planes, per-lane alignment tests cost 28.3 -> 32.7 us)
+        sp.vec_reads = esz == 2 && HW % W == 0 && (HW / W) % (1 << tl) == 0;
+        const int red = kThreads * sp.cpl * 2 * static_cast<int>(sizeof(float));
         sp.smem = 2 * sp.R * slot > red ? 2 * sp.R * slot : red;
-        sp.S = bulk_slices((C + G - 1) / G, P, C, sp.smem);
+        sp.S = bulk_slices((C + G - 1) / G, P, C, sp.smem, sp.cpl);
     } else if (sp.kind == kStaged) {
         sp.G = G;
         sp.slot_bytes = slot;
@@ -1021,7 +1086,131 @@ int launch_apply(const BnParams& p, int cmode, bool nc, dim3 grid, cudaStream_t 
     if (cmode == 0) return launch_apply_mode<BF16_IN, BF16_OUT, 0>(p, nc, grid, s);
     if (cmode == 1) return launch_apply_mode<BF16_IN, BF16_OUT, 1>(p, nc, grid, s);
     if (cmode == 3) return launch_apply_mode<BF16_IN, BF16_OUT, 3>(p, nc, grid, s);
+    if (cmode == 4) return launch_apply_mode<BF16_IN, BF16_OUT, 4>(p, nc, grid, s);
     return launch_apply_mode<BF16_IN, BF16_OUT, 2>(p, nc, grid, s);
+}
+
+// Whether a call runs as two channel halves on two streams: aligned planes
+// (plane statistics, apply mode 0), an even channel count and an input large
+// enough that three short launches leave the memory idle between them.
+// Measured on 8 x [32, C, H, W] bf16 as two half-size calls on two streams:
+// 64x56x56 46.2 -> 44.8 us, 256x56x56 188.6 -> 180.8, 512x28x28 95.8 -> 91.5;
+// 2048x7x7 (bulk statistics) gained nothing.  Both halves use one slice
+// count, fitted to the half's grid, so the sums, and every output bit, are
+// those of the call run as one sequence with that count.
+constexpr int64_t kSplitMinBytes = int64_t(16) << 20;   // x over all replicas
+constexpr int kSplitMinChannels = 16;                     // per half
+
+bool split_channels(const StatsPlan& sp, int n, int batch, int C, int HW, int esz) {
+    return sp.kind == kPlaneVec && HW % 8 == 0 && C % 2 == 0 && C / 2 >= kSplitMinChannels &&
+           static_cast<int64_t>(n) * batch * C * HW * esz >= kSplitMinBytes;
+}
+
+// A side stream and its fork and join events, one per host thread and
+// device, created on the thread's first split call outside stream capture
+// (a call that finds none while its stream is capturing runs unsplit, with
+// the same results).  Destroyed when the thread exits; stale after
+// cudaDeviceReset.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    ~SideStream() {
+        if (s) cudaStreamDestroy(s);
+        if (fork) cudaEventDestroy(fork);
+        if (join) cudaEventDestroy(join);
+    }
+};
+constexpr int kMaxSideDevices = 64;
+
+SideStream* side_stream(cudaStream_t caller) {
+    thread_local SideStream table[kMaxSideDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+    SideStream& h = table[dev];
+    if (h.s != nullptr) return &h;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+        if (st) cudaStreamDestroy(st);
+        if (f) cudaEventDestroy(f);
+        return nullptr;
+    }
+    h.s = st;
+    h.fork = f;
+    h.join = j;
+    return &h;
+}
+
+// The three launches of a call (statistics, merge, apply) for the channels
+// [p.c_base, p.c_end), on stream s.
+int launch_sequence(BnParams p, const StatsPlan& sp, bool bf16_in, bool bf16_out, bool nc, cudaStream_t s) {
+    int st;
+    if (sp.kind == kBulk || sp.kind == kStaged) {
+        p.div_unit = make_fastdiv(static_cast<uint32_t>(sp.slot_bytes / 16));
+        const dim3 grid(static_cast<unsigned>((p.C + sp.G - 1) / sp.G), static_cast<unsigned>(sp.S));
+        if (sp.kind == kBulk)
+            st = bf16_in ? launch_bulk<true>(sp.cpl, grid, sp.smem, s, p) : launch_bulk<false>(sp.cpl, grid, sp.smem, s, p);
+        else
+            st = bf16_in ? launch_pdl(bn_stats_group_kernel<true>, grid, kThreads, s, p)
+                         : launch_pdl(bn_stats_group_kernel<false>, grid, kThreads, s, p);
+    } else {
+        const int wv = bf16_in ? 8 : 4;             // elements per 16-byte vector
+        const dim3 grid(static_cast<unsigned>(p.c_end - p.c_base), static_cast<unsigned>(sp.S));
+        if (sp.kind == kPlaneVec) {
+            const uint32_t units = static_cast<uint32_t>(p.HW / wv);
+            p.div_unit = make_fastdiv((units + kChunkVecs - 1) / kChunkVecs);
+            st = bf16_in ? launch_pdl(bn_stats_plane_kernel<true>, grid, kThreads, s, p)
+                         : launch_pdl(bn_stats_plane_kernel<false>, grid, kThreads, s, p);
+        } else {
+            st = bf16_in ? launch_pdl(bn_stats_element_kernel<true>, grid, kThreads, s, p)
+                         : launch_pdl(bn_stats_element_kernel<false>, grid, kThreads, s, p);
+        }
+    }
+    if (st != DDP_OK) return st;
+    const dim3 mgrid(static_cast<unsigned>((p.c_end - p.c_base + 31) / 32));
+    st = bf16_in ? launch_pdl(bn_merge_kernel<true>, mgrid, kMergeThreads, s, p)
+                 : launch_pdl(bn_merge_kernel<false>, mgrid, kMergeThreads, s, p);
+    if (st != DDP_OK) return st;
+
+    DeviceInfo d;
+    if ((st = current_device_info(&d)) != DDP_OK) return st;
+    const int64_t nvec = static_cast<int64_t>(p.batch) * (p.c_end - p.c_base) * p.HW / 8;
+    // at least kApplyVecs vectors per thread (two passes of its 4-vector unroll), and at most
+    // kApplyWaves waves counted at the SM's thread limit (8 CTAs of 256 threads; registers
+    // allow 5-6, so the grid runs more real waves): several waves stream faster than one
+    // grid-stride wave, and grids rounded to whole real waves measured slower
+    int64_t gx = (nvec + static_cast<int64_t>(kThreads) * kApplyVecs - 1) / (static_cast<int64_t>(kThreads) * kApplyVecs);
+    const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
+    int64_t cap = (kApplyWaves * resident + p.n - 1) / p.n;
+    if (gx > cap) gx = cap;
+    if (gx < 1) gx = 1;
+    int cmode = (p.HW % 8) == 0 ? (p.parted ? 4 : 0) : (p.HW >= 8 ? 1 : 2);
+    if (cmode == 1 && (static_cast<int64_t>(p.C) * p.HW) % 8 == 0) {
+        // mode 3: a grid stride (gx*kThreads vectors) that is a whole number of samples, with gx the
+        // multiple of the smallest such count nearest to the size chosen above
+        const int64_t vs8 = static_cast<int64_t>(p.C) * p.HW / 8;
+        int64_t gcd = kThreads, tmp = vs8;
+        while (tmp != 0) {                                  // gcd(kThreads, vs8)
+            const int64_t q = gcd % tmp;
+            gcd = tmp;
+            tmp = q;
+        }
+        const int64_t m0 = vs8 / gcd;                       // CTAs per whole number of samples
+        int64_t g3 = (gx + m0 / 2) / m0 * m0;
+        if (g3 < m0) g3 = m0;
+        if (g3 <= 2 * gx + m0 && g3 * kThreads <= (int64_t(1) << 31) / 4) {
+            gx = g3;
+            cmode = 3;
+            p.div_vs8 = make_fastdiv(static_cast<uint32_t>(vs8));
+        }
+    }
+    const dim3 agrid(static_cast<unsigned>(gx), static_cast<unsigned>(p.n));
+    if (bf16_in) return bf16_out ? launch_apply<true, true>(p, cmode, nc, agrid, s) : launch_apply<true, false>(p, cmode, nc, agrid, s);
+    return bf16_out ? launch_apply<false, true>(p, cmode, nc, agrid, s) : launch_apply<false, false>(p, cmode, nc, agrid, s);
 }
 
 }  // namespace
@@ -1033,6 +1222,15 @@ extern "C" size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int3
     if (!valid_sizes(n_replicas, batch, C, H, W)) return 0;
     const int64_t parts = max_partials(n_replicas, batch, C, H * W);
     return align_up(static_cast<size_t>(parts) * sizeof(float2), 16) + static_cast<size_t>(C) * sizeof(float4);
+}
+
+extern "C" int syncbn_channel_parts(int32_t n_replicas, int32_t in_dtype, int32_t batch, int32_t C, int32_t H,
+                                    int32_t W) {
+    if (!valid_sizes(n_replicas, batch, C, H, W) || (in_dtype != DDP_F32 && in_dtype != DDP_BF16))
+        return DDP_ERR_INVALID_ARG;
+    const int esz = in_dtype == DDP_BF16 ? 2 : 4;
+    const StatsPlan sp = plan_stats(n_replicas, batch, C, H * W, esz);
+    return split_channels(sp, n_replicas, batch, C, H * W, esz) ? 2 : 1;
 }
 
 extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtype,
@@ -1073,6 +1271,7 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     const bool bf16_in = in_dtype == DDP_BF16;
     const int esz = bf16_in ? 2 : 4;
     StatsPlan sp = plan_stats(n_replicas, batch, C, H * W, esz);
+    const bool split = split_channels(sp, n_replicas, batch, C, H * W, esz);
     int st;
     if (sp.kind == kPlaneVec) {
         // the plan's slice count sizes the workspace; the launch may take fewer to end on a full wave
@@ -1083,7 +1282,9 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
                                             : reinterpret_cast<const void*>(bn_stats_plane_kernel<false>),
                                     kThreads, &per_sm);
         if (st != DDP_OK) return st;
-        sp.S = plane_slices_for_wave(C, sp.S, static_cast<int64_t>(d.sm_count) * per_sm);
+        // a split call fits the wave of each half, and runs with that slice count also where it
+        // finds no side stream (then as one sequence, with the same sums)
+        sp.S = plane_slices_for_wave(split ? C / 2 : C, sp.S, static_cast<int64_t>(d.sm_count) * per_sm);
     }
 
     BnParams p{};
@@ -1104,8 +1305,8 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     p.R = sp.R;
     p.slot_bytes = sp.slot_bytes;
     p.buf_fl = (static_cast<uint64_t>(batch) * C * p.HW * esz) & ~uint64_t(15);
-    p.tc_log2 = 0;
-    while (sp.G < 32 && (sp.G << p.tc_log2) < 32) ++p.tc_log2;
+    p.tc_log2 = sp.tc_log2;
+    p.vec_reads = sp.vec_reads ? 1 : 0;
     p.eps = eps;
     const double inv_count = 1.0 / (static_cast<double>(n_replicas) * batch * p.HW);
     p.inv_hi = static_cast<float>(inv_count);
@@ -1125,70 +1326,37 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     p.div_c = make_fastdiv(static_cast<uint32_t>(C));
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (sp.kind == kBulk || sp.kind == kStaged) {
-        p.div_unit = make_fastdiv(static_cast<uint32_t>(sp.slot_bytes / 16));
-        const dim3 grid(static_cast<unsigned>((C + sp.G - 1) / sp.G), static_cast<unsigned>(sp.S));
-        if (sp.kind == kBulk)
-            st = bf16_in ? launch_bulk<true>(sp.G, grid, sp.smem, s, p) : launch_bulk<false>(sp.G, grid, sp.smem, s, p);
-        else
-            st = bf16_in ? launch_pdl(bn_stats_group_kernel<true>, grid, kThreads, s, p)
-                         : launch_pdl(bn_stats_group_kernel<false>, grid, kThreads, s, p);
-    } else {
-        const int wv = 16 / esz;
-        const dim3 grid(static_cast<unsigned>(C), static_cast<unsigned>(sp.S));
-        if (sp.kind == kPlaneVec) {
-            const uint32_t units = static_cast<uint32_t>(p.HW / wv);
-            p.div_unit = make_fastdiv((units + kChunkVecs - 1) / kChunkVecs);
-            st = bf16_in ? launch_pdl(bn_stats_plane_kernel<true>, grid, kThreads, s, p)
-                         : launch_pdl(bn_stats_plane_kernel<false>, grid, kThreads, s, p);
-        } else {
-            st = bf16_in ? launch_pdl(bn_stats_element_kernel<true>, grid, kThreads, s, p)
-                         : launch_pdl(bn_stats_element_kernel<false>, grid, kThreads, s, p);
-        }
-    }
-    if (st != DDP_OK) return st;
-    const dim3 mgrid(static_cast<unsigned>((C + 31) / 32));
-    st = bf16_in ? launch_pdl(bn_merge_kernel<true>, mgrid, kMergeThreads, s, p)
-                 : launch_pdl(bn_merge_kernel<false>, mgrid, kMergeThreads, s, p);
-    if (st != DDP_OK) return st;
-
-    DeviceInfo d;
-    if ((st = current_device_info(&d)) != DDP_OK) return st;
-    const int64_t nvec = static_cast<int64_t>(E / 8);
-    // at least kApplyVecs vectors per thread (two passes of its 4-vector unroll), and at most
-    // kApplyWaves waves counted at the SM's thread limit (8 CTAs of 256 threads; registers
-    // allow 5-6, so the grid runs more real waves): several waves stream faster than one
-    // grid-stride wave, and grids rounded to whole real waves measured slower
-    int64_t gx = (nvec + static_cast<int64_t>(kThreads) * kApplyVecs - 1) / (static_cast<int64_t>(kThreads) * kApplyVecs);
-    const int64_t resident = static_cast<int64_t>(d.sm_count) * (d.max_threads_per_sm / kThreads);
-    int64_t cap = (kApplyWaves * resident + n_replicas - 1) / n_replicas;
-    if (gx > cap) gx = cap;
-    if (gx < 1) gx = 1;
-    int cmode = (p.HW % 8) == 0 ? 0 : (p.HW >= 8 ? 1 : 2);
-    if (cmode == 1 && (static_cast<int64_t>(C) * p.HW) % 8 == 0) {
-        // mode 3: a grid stride (gx*kThreads vectors) that is a whole number of samples, with gx the
-        // multiple of the smallest such count nearest to the size chosen above
-        const int64_t vs8 = static_cast<int64_t>(C) * p.HW / 8;
-        int64_t gcd = kThreads, tmp = vs8;
-        while (tmp != 0) {                                  // gcd(kThreads, vs8)
-            const int64_t q = gcd % tmp;
-            gcd = tmp;
-            tmp = q;
-        }
-        const int64_t m0 = vs8 / gcd;                       // CTAs per whole number of samples
-        int64_t g3 = (gx + m0 / 2) / m0 * m0;
-        if (g3 < m0) g3 = m0;
-        if (g3 <= 2 * gx + m0 && g3 * kThreads <= (int64_t(1) << 31) / 4) {
-            gx = g3;
-            cmode = 3;
-            p.div_vs8 = make_fastdiv(static_cast<uint32_t>(vs8));
-        }
-    }
-    const dim3 agrid(static_cast<unsigned>(gx), static_cast<unsigned>(n_replicas));
     const bool nc = !in_place_any;
     const bool bf16_out = out_dtype == DDP_BF16;
-    if (bf16_in) return bf16_out ? launch_apply<true, true>(p, cmode, nc, agrid, s) : launch_apply<true, false>(p, cmode, nc, agrid, s);
-    return bf16_out ? launch_apply<false, true>(p, cmode, nc, agrid, s) : launch_apply<false, false>(p, cmode, nc, agrid, s);
+    p.c_base = 0;
+    p.c_end = C;
+    SideStream* side = nullptr;
+    if (split) side = side_stream(s);
+    if (side == nullptr) return launch_sequence(p, sp, bf16_in, bf16_out, nc, s);
+
+    // two channel halves, the second on the side stream: each half's merge and apply overlap the
+    // other's statistics and apply instead of leaving the memory idle between the launches
+    BnParams q = p;
+    const int half = C / 2;
+    p.c_end = half;
+    q.c_base = half;
+    for (BnParams* h : {&p, &q}) {
+        h->parted = 1;
+        h->div_vp = make_fastdiv(static_cast<uint32_t>(static_cast<int64_t>(half) * p.HW / 8));
+        h->vs_full = static_cast<uint32_t>(static_cast<int64_t>(C) * p.HW / 8);
+        h->v_base = static_cast<uint32_t>(static_cast<int64_t>(h->c_base) * p.HW / 8);
+    }
+    cudaError_t e = cudaEventRecord(side->fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(side->s, side->fork, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st = launch_sequence(p, sp, bf16_in, bf16_out, nc, s);
+    if (st == DDP_OK) st = launch_sequence(q, sp, bf16_in, bf16_out, nc, side->s);
+    // the join is recorded whatever happened, so that the caller's stream (or its capture) never
+    // leaves the side stream's work unjoined
+    e = cudaEventRecord(side->join, side->s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, side->join, 0);
+    if (st != DDP_OK) return st;
+    return e == cudaSuccess ? DDP_OK : cuda_fail(e);
 }
 
 // ---------------------------------------------------------------- variant without a caller workspace

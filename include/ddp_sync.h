@@ -395,6 +395,17 @@ int ddp_bucket_allreduce_sgd_cast(const void* const* replicas, int32_t n_replica
 size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int32_t H, int32_t W);
 
 /*
+ * syncbn_channel_parts — how syncbn_merge_apply runs these sizes: 2 when it
+ * splits the channels into two halves on two streams (see "Streams" under
+ * syncbn_merge_apply; each half is three launches), 1 when it runs one
+ * sequence of three launches on the caller's stream, DDP_ERR_INVALID_ARG
+ * for invalid sizes or dtype.  A call that finds no side stream of its
+ * thread while its stream captures runs one sequence even where this
+ * returns 2.
+ */
+int syncbn_channel_parts(int32_t n_replicas, int32_t in_dtype, int32_t batch, int32_t C, int32_t H, int32_t W);
+
+/*
  * syncbn_merge_apply — strict SyncBatchNorm forward across N replicas.
  *
  * [TR24] §十二: strict SyncBatchNorm all-reduces each rank's per-channel sum
@@ -425,6 +436,14 @@ size_t syncbn_workspace_bytes(int32_t n_replicas, int32_t batch, int32_t C, int3
  *                kernels may overlap on the GPU (different streams without
  *                ordering) need different workspaces, or they race on the
  *                partial sums
+ * Streams: large inputs with H*W a multiple of 8 and an even C run as two
+ * channel halves, the second on a side stream that the library keeps per
+ * host thread and device (created on the thread's first such call made
+ * outside stream capture; a call that finds none while its stream captures
+ * runs as one sequence).  The side stream waits on an event recorded on
+ * `stream` and `stream` waits on its join event before the call returns,
+ * so the call stays ordered on `stream` and capturable; both forms give the
+ * same bits.  After cudaDeviceReset the thread's side stream is stale.
  */
 int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtype,
                        int32_t batch, int32_t C, int32_t H, int32_t W, float eps,

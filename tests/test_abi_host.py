@@ -307,3 +307,26 @@ def test_mean_multi_rejects(g):
     assert f(two, 2, 0, a, 0, out, None) == g.DDP_OK
     a5, keep5 = bk((0, 0), (64, 0))
     assert f(two, 2, 0, a5, 2, out, None) == g.DDP_OK                  # empty buckets only
+
+
+def test_syncbn_channel_parts(g):
+    """Which SyncBN calls run as two channel halves on two streams: aligned
+    planes with the plane statistics kernel (H*W a multiple of 8 and, for
+    bf16, at least 16 vectors), an even C of at least 32 and 16 MiB of input
+    over all replicas.  The planner decides on the host, no GPU needed."""
+    bf16, f32 = g.BF16, g.F32
+    assert g.syncbn_channel_parts(8, bf16, 32, 64, 56, 56) == 2
+    assert g.syncbn_channel_parts(8, bf16, 32, 256, 56, 56) == 2
+    assert g.syncbn_channel_parts(8, bf16, 32, 512, 28, 28) == 2
+    assert g.syncbn_channel_parts(8, bf16, 32, 2048, 7, 7) == 1       # unaligned: bulk-staged statistics
+    assert g.syncbn_channel_parts(8, bf16, 32, 2048, 8, 8) == 1       # 8 vectors per plane: bulk-staged
+    assert g.syncbn_channel_parts(8, f32, 32, 2048, 8, 8) == 2        # fp32: plane kernel, 16 vectors
+    assert g.syncbn_channel_parts(8, bf16, 32, 65, 56, 56) == 1       # odd C
+    assert g.syncbn_channel_parts(8, bf16, 32, 30, 56, 56) == 1       # 15 channels per half
+    assert g.syncbn_channel_parts(8, bf16, 32, 32, 56, 56) == 2       # 16 per half, 51 MB
+    assert g.syncbn_channel_parts(2, bf16, 32, 32, 56, 56) == 1       # 12.8 MB: under 16 MiB
+    assert g.syncbn_channel_parts(8, bf16, 32, 64, 28, 29) == 1       # H*W = 812: not a multiple of 8
+    for bad in [(0, bf16, 32, 64, 56, 56), (17, bf16, 32, 64, 56, 56), (8, 7, 32, 64, 56, 56),
+                (8, bf16, 0, 64, 56, 56), (8, bf16, 32, 64, 0, 56)]:
+        with pytest.raises(RuntimeError):
+            g.syncbn_channel_parts(*bad)

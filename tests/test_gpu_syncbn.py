@@ -85,7 +85,8 @@ def _run(g, xs_dev, ys_dev, C, eps=1e-5, gamma=None, beta=None):
                                    (2, 2, 70, 3, 7), (2, 2, 300, 1, 5), (3, 2, 260, 1, 7),
                                    (2, 3, 4, 67, 8), (5, 3, 24, 7, 7), (2, 3, 12, 14, 14), (6, 5, 32, 5, 5),
                                    (3, 7, 40, 28, 28), (16, 2, 8, 56, 56), (2, 2, 40000, 2, 4),
-                                   (2, 2, 512, 14, 14), (2, 1, 2048, 7, 7)])
+                                   (2, 2, 512, 14, 14), (2, 1, 2048, 7, 7), (2, 3, 300, 4, 4), (2, 3, 200, 4, 8),
+                                   (3, 2, 100, 8, 8)])
 @pytest.mark.parametrize("io", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "f32"), ("f32", "bf16")])
 def test_small_shapes(g, shape, io):
     n, B, C, H, W = shape
@@ -181,7 +182,8 @@ def test_large_mean_small_std(g):
 
 @pytest.mark.parametrize("shape,in_place", [((8, 32, 128, 28, 28), False), ((8, 32, 256, 14, 14), False),
                                             ((8, 32, 128, 28, 28), True), ((8, 32, 256, 14, 14), True),
-                                            ((8, 32, 2048, 7, 7), True)])
+                                            ((8, 32, 2048, 7, 7), True), ((8, 32, 256, 28, 28), False),
+                                            ((8, 32, 256, 28, 28), True)])
 def test_chained_layers_equal_separate_calls(g, shape, in_place):
     """Three SyncBN calls back to back on one stream, each reading the
     previous call's output: a call's apply reads its first vectors of x
@@ -189,8 +191,9 @@ def test_chained_layers_equal_separate_calls(g, shape, in_place):
     call's apply has written that x.  The chained result equals, bit for
     bit, the same three calls each followed by a device synchronisation
     (the kernels' reduction orders are fixed, so equal inputs give equal
-    bits).  Aligned 28x28 planes (plane statistics) and unaligned 14x14
-    planes (bulk-staged statistics), out of place and in place."""
+    bits).  Aligned 28x28 planes (plane statistics; with 256 channels the
+    call runs as two channel halves on two streams) and unaligned 14x14 and
+    7x7 planes (bulk-staged statistics), out of place and in place."""
     n, B, C, H, W = shape
     xs = [dev_bf16(x) for x in workloads.syncbn_input(4, n, B, C, H, W)]
     ws = torch.empty(g.syncbn_workspace_bytes(n, B, C, H, W), dtype=torch.uint8, device="cuda")
@@ -216,13 +219,14 @@ def test_chained_layers_equal_separate_calls(g, shape, in_place):
             assert torch.equal(got[r].view(torch.int16), sep[r].view(torch.int16)), f"replica {r}"
 
 
-@pytest.mark.parametrize("shape", [(4, 2, 6, 8, 8), (4, 2, 6, 7, 7)])
+@pytest.mark.parametrize("shape", [(4, 2, 6, 8, 8), (4, 2, 6, 7, 7), (4, 2, 6, 16, 32)])
 def test_non_finite_channel_stays_in_its_channel(g, shape):
     """A NaN in channel 1 and an infinity in channel 4 of one replica: those
     channels' statistics are not finite (the oracle's are not either), and
     every other channel's mean, invstd and output match the oracle, so a
     non-finite activation reaches no other channel (aligned 8x8 and
-    unaligned 7x7 planes)."""
+    unaligned 7x7 planes: bulk-staged statistics; aligned 16x32 planes:
+    plane statistics)."""
     n, B, C, H, W = shape
     xs = workloads.syncbn_input(4, n, B, C, H, W)
     xs[2][1, 1, 3, 2] = 0x7FC0          # NaN

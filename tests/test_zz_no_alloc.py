@@ -12,11 +12,11 @@ Three calls in a row on different shapes, each checked twice:
   * against the fp64 oracle on a few channels, with the tolerances of the
     SyncBN parity tests.
 The shapes go from a small footprint (64 channels of 14x14: bulk-staged
-statistics) to a large one (40000 channels of 2x4 planes: the plane
-statistics kernel, whose launch may use fewer slices than the workspace is
-sized for) and back to a smaller one (2048 channels of 7x7: bulk-staged
-statistics), so leftover contents of the array are exercised in both
-directions, through two different statistics kernels.
+statistics) to a large one (16000 channels of 16x32 planes: the plane
+statistics kernel, the call run as two channel halves on two streams) and
+back to a smaller one (2048 channels of 7x7: bulk-staged statistics), so
+leftover contents of the array are exercised in both directions, through
+two different statistics kernels.
 
 This file is collected last so that a run stopping at the first failure has
 already run every other test.
@@ -86,7 +86,7 @@ def test_noalloc_matches_workspace_entry_three_calls():
     f = _entry(g)
     stream = torch.cuda.current_stream().cuda_stream
 
-    shapes = [(8, 4, 64, 14, 14, 1), (2, 2, 40000, 2, 4, 2), (4, 2, 2048, 7, 7, 3)]
+    shapes = [(8, 4, 64, 14, 14, 1), (2, 2, 16000, 16, 32, 2), (4, 2, 2048, 7, 7, 3)]
     for call, (n, B, C, H, W, seed) in enumerate(shapes):
         xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, 900 + 10 * seed + r, dtype=torch.bfloat16)
               for r in range(n)]
