@@ -1,17 +1,19 @@
 """SyncBN calls that run as two channel halves on two streams.
 
-Large calls on aligned planes (H*W a multiple of 8, even C, at least 64 MiB
-of input over all replicas) run the statistics, merge and apply of channels
-[0, C/2) on the caller's stream and those of [C/2, C) on a side stream that
-the library keeps per host thread and device, joined back before the call
-returns.  Both halves use the whole call's slice count, so the split call
-and the call run as one sequence give the same bits: a thread's first call
-made inside a stream capture, which finds no side stream yet, runs as one
-sequence, and its replay must equal the split call bit for bit.  The
-statistics themselves are checked against the oracle on every channel by
-the full-size tests of the SyncBN parity file; here: the split call against
-the oracle on a few channels, in a graph, from several threads at once, and
-chained in place.
+Calls on aligned planes that take the plane statistics kernel (H*W a
+multiple of 8), with an even C of at least 32 and at least 16 MiB of input
+over all replicas, run the statistics, merge and apply of channels [0, C/2)
+on the caller's stream and those of [C/2, C) on a side stream that the
+library keeps per host thread and device, joined back before the call
+returns.  Both halves use one slice count, so the split call and the call
+run as one sequence give the same bits: a thread's first call made inside a
+stream capture, which finds no side stream yet, runs as one sequence, and
+its replay must equal the split call bit for bit.  The statistics are
+checked against the oracle on every channel by the full-size tests of the
+SyncBN parity file; here: the split call against the oracle on a few
+channels for every input and output dtype, in a graph, from a capture that
+runs unsplit, and from several threads at once (chained in place: the
+SyncBN parity file).
 """
 import threading
 
@@ -56,38 +58,56 @@ def _bf16_ulp(v):
 
 def _check_channels(xs, ys, m, s, gamma, beta, chans, what):
     """fp64 oracle on channels `chans`: mean within 1e-5 relative + 1e-7
-    standard deviations, invstd within 1e-5 relative, y within one bf16 ulp
-    of the oracle's value rounded to bf16 plus 1e-5 relative + 1e-6."""
+    standard deviations, invstd within 1e-5 relative; y within 1e-5 relative
+    + 1e-6 of the fp64 value (fp32 output), or within one bf16 ulp of that
+    value rounded to bf16 plus the same allowance (bf16 output)."""
     m_all, s_all = m.cpu().numpy().astype(np.float64), s.cpu().numpy().astype(np.float64)
     g_h = gamma.cpu().numpy().astype(np.float64) if gamma is not None else None
     b_h = beta.cpu().numpy().astype(np.float64) if beta is not None else None
+    f32_in = xs[0].dtype == torch.float32
     for c in chans:
-        xc = [x[:, c].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, 1) for x in xs]
-        m_w, s_w = oracle.syncbn_stats_at(xc, 0, 1e-5)
+        if f32_in:
+            xc = [x[:, c].contiguous().cpu().numpy().reshape(-1, 1) for x in xs]
+            m_w, s_w = oracle.syncbn_stats_at(xc, 0, 1e-5, dtype="f32")
+        else:
+            xc = [x[:, c].contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1, 1) for x in xs]
+            m_w, s_w = oracle.syncbn_stats_at(xc, 0, 1e-5)
         assert abs(m_all[c] - m_w) <= 1e-5 * abs(m_w) + 1e-7 / s_w, (what, c, m_all[c], m_w)
         assert abs(s_all[c] - s_w) <= 1e-5 * s_w, (what, c, s_all[c], s_w)
         gc = g_h[c] if g_h is not None else 1.0
         bc = b_h[c] if b_h is not None else 0.0
         for r in range(len(xs)):
-            xv = oracle.bf16_bits_to_f32(xc[r][:, 0]).astype(np.float64)
+            xv = (xc[r][:, 0] if f32_in else oracle.bf16_bits_to_f32(xc[r][:, 0])).astype(np.float64)
             y_w = (xv - m_w) * s_w * gc + bc
-            want = oracle.f64_to_bf16_rne(y_w)
             got = ys[r][:, c].float().cpu().numpy().reshape(-1).astype(np.float64)
-            tol = _bf16_ulp(want) * 1.0001 + 1e-5 * np.abs(y_w) + 1e-6
+            if ys[r].dtype == torch.bfloat16:
+                want = oracle.f64_to_bf16_rne(y_w)
+                tol = _bf16_ulp(want) * 1.0001 + 1e-5 * np.abs(y_w) + 1e-6
+            else:
+                want = y_w
+                tol = 1e-5 * np.abs(y_w) + 1e-6
             assert np.all(np.abs(got - want) <= tol), (what, c, r)
 
 
-def test_split_call_matches_oracle(g):
+@pytest.mark.parametrize("io", [("bf16", "bf16"), ("bf16", "f32"), ("f32", "f32"), ("f32", "bf16")])
+def test_split_call_matches_oracle(g, io):
     n, B, C, H, W = SHAPE
-    xs = _inputs(SHAPE, 1000)
+    if io[0] == "f32":
+        B = B // 2                       # fp32: the same 103 MB of input
+        xs = [workloads.device_normal((B, C, H, W), 0.5, 2.0, 1000 + r) for r in range(n)]
+    else:
+        xs = _inputs(SHAPE, 1000)
+    assert g.syncbn_channel_parts(n, g.F32 if io[0] == "f32" else g.BF16, B, C, H, W) == 2
     gamma = workloads.device_normal((C,), 1.0, 0.1, 1100)
     beta = workloads.device_normal((C,), 0.0, 0.1, 1101)
-    ys, m, s = _outputs(xs, C)
+    odt = torch.float32 if io[1] == "f32" else torch.bfloat16
+    ys = [torch.full(x.shape, float("nan"), dtype=odt, device="cuda") for x in xs]
+    m, s = torch.full((C,), float("nan"), device="cuda"), torch.full((C,), float("nan"), device="cuda")
     ws = torch.empty(g.syncbn_workspace_bytes(n, B, C, H, W), dtype=torch.uint8, device="cuda")
     g.syncbn_merge_apply(xs, ys, m, s, ws, 1e-5, gamma, beta)
     sync()
     # both halves' first and last channels and one inside each
-    _check_channels(xs, ys, m, s, gamma, beta, [0, 13, C // 2 - 1, C // 2, C // 2 + 17, C - 1], "split call")
+    _check_channels(xs, ys, m, s, gamma, beta, [0, 13, C // 2 - 1, C // 2, C // 2 + 17, C - 1], f"split call {io}")
 
 
 def test_split_call_in_graph_matches_eager(g):
