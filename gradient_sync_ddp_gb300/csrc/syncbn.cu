@@ -891,7 +891,7 @@ int launch_pdl_smem(void (*kernel)(BnParams), dim3 grid, int smem, cudaStream_t 
     return check_launch();
 }
 
-// Channels per lane of the bulk-staged kernel: G/32 for G >= 32 (G <= 256).
+// Channels per lane of the bulk-staged kernel: G * (lanes per channel) / 32.
 template <bool BF16>
 int launch_bulk(int cpl, dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
     switch (cpl) {
@@ -1093,11 +1093,13 @@ int launch_apply(const BnParams& p, int cmode, bool nc, dim3 grid, cudaStream_t 
 // Whether a call runs as two channel halves on two streams: aligned planes
 // (plane statistics, apply mode 0), an even channel count and an input large
 // enough that three short launches leave the memory idle between them.
-// Measured on 8 x [32, C, H, W] bf16 as two half-size calls on two streams:
-// 64x56x56 46.2 -> 44.8 us, 256x56x56 188.6 -> 180.8, 512x28x28 95.8 -> 91.5;
-// 2048x7x7 (bulk statistics) gained nothing.  Both halves use one slice
-// count, fitted to the half's grid, so the sums, and every output bit, are
-// those of the call run as one sequence with that count.
+// Measured on 8 x [32, C, H, W] bf16 with inputs rotated past L2 (us per
+// call, one sequence -> two halves): 64x56x56 46.1 -> 45.5, 256x56x56
+// 188.5 -> 181.9, 512x28x28 95.9 -> 92.0, 64x28x28 22.9 -> 19.7; as two
+// independent half-size calls, 2048x7x7 (bulk statistics) gained nothing.
+// Both halves use one slice count, fitted to the half's grid, so the sums,
+// and every output bit, are those of the call run as one sequence with
+// that count.
 constexpr int64_t kSplitMinBytes = int64_t(16) << 20;   // x over all replicas
 constexpr int kSplitMinChannels = 16;                     // per half
 
@@ -1125,16 +1127,26 @@ constexpr int kMaxSideDevices = 64;
 SideStream* side_stream(cudaStream_t caller) {
     thread_local SideStream table[kMaxSideDevices];
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxSideDevices) return nullptr;
     SideStream& h = table[dev];
     if (h.s != nullptr) return &h;
+    // a failed query or creation leaves no error behind for the launches' own checks to report
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+    if (cudaStreamIsCapturing(caller, &cs) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return nullptr;
     cudaStream_t st = nullptr;
     cudaEvent_t f = nullptr, j = nullptr;
     if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
         cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+        (void)cudaGetLastError();
         if (st) cudaStreamDestroy(st);
         if (f) cudaEventDestroy(f);
         return nullptr;
