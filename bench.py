@@ -49,12 +49,16 @@ L2_BYTES = 129 * 10 ** 6
 # finalizer of (half xor round key) masked and xored into the other half: 2 multiplies, 3 shifts
 # and 6 logic operations; the cycle walk then composes the value (1 multiply-add) and compares it
 # with n (1): 46 integer operations per encryption.  Cycle walking takes 2^bits / n encryptions per
-# index on average (bits = ceil(log2 n): the domain over the values in range).  Each SM issues 4
-# warp instructions (128 lanes) per cycle, and its two integer-capable pipes (ALU: logic, shifts,
-# compares; FMA-heavy: multiplies, and shifts written as multiply-highs) take 64 lanes per cycle
-# each: at best 128 integer operations per SM cycle.
+# index on average (bits = ceil(log2 n): the domain over the values in range).  An SM has two
+# integer-capable pipes of 64 lanes per cycle each: the ALU (logic operations, compares, shifts)
+# and the FMA-heavy pipe (multiplies, multiply-adds, and shifts written as multiply-highs).  The
+# 25 logic operations and compares can issue only on the ALU and the 9 multiplies only on the
+# other pipe; the 12 shifts can go to either, so the best split puts them all on the FMA-heavy
+# pipe (21 operations there) and the ALU's 25 set the pace: max(25, 46 / 2) / 64 SM cycles per
+# encryption.
 SAMPLER_OPS_PER_ENCRYPTION = 4 * (2 + 3 + 6) + 2
-SAMPLER_OPS_PER_SM_CYCLE = 128
+SAMPLER_ALU_ONLY_OPS = 4 * 6 + 1
+SAMPLER_PIPE_LANES = 64
 GB300_SMS = 152
 STEP_STREAMS = 8       # streams the headline step's bucket launches are spread over
 SYNCBN_CALLS = 12      # calls captured per graph in the SyncBN rows (a multiple of every input-set count)
@@ -818,19 +822,22 @@ def bench_rows(g, torch, dev, peak, peak_kind, only=None, rows_out=None):
         out = torch.empty(N * g.dist_sampler_num_samples(n, N, False), dtype=torch.int64, device=dev)
         ms = _time_launches(torch, lambda: [g.dist_sampler_indices(n, N, -1, 0, 1 + e, True, False, out)
                                             for e in range(SAMPLER_CALLS)], 10, side) / SAMPLER_CALLS
-        # Integer roofline from the arithmetic (SAMPLER_OPS_PER_ENCRYPTION), at the maximum SM clock
+        # Integer roofline from the arithmetic (the ops of one encryption on the ALU and FMA-heavy
+        # pipes), at the maximum SM clock
         bits = max(1, (n - 1).bit_length())
         enc_per_index = (1 << bits) / n
         sm_hz = 2.07e9
-        peak_idx = GB300_SMS * SAMPLER_OPS_PER_SM_CYCLE * sm_hz / (SAMPLER_OPS_PER_ENCRYPTION * enc_per_index)
+        pipe_ops = max(SAMPLER_ALU_ONLY_OPS, SAMPLER_OPS_PER_ENCRYPTION / 2)   # busiest pipe's ops per encryption
+        peak_idx = GB300_SMS * SAMPLER_PIPE_LANES * sm_hz / (pipe_ops * enc_per_index)
         idx_per_s = out.numel() / (ms * 1e-3)
         emit_row("sampler_imagenet", {"workload": "1,281,167 items, 8 ranks, all ranks, shuffle", "ms": ms,
                                       "Mindex_per_s": idx_per_s / 1e6, "bytes": out.numel() * 8,
                                       "GBps": out.numel() * 8 / ms / 1e6, "bound": "alu",
                                       "peak_Mindex_per_s": peak_idx / 1e6, "frac": idx_per_s / peak_idx,
-                                      "peak_basis": f"{SAMPLER_OPS_PER_ENCRYPTION} integer ops per encryption x "
+                                      "peak_basis": f"{SAMPLER_OPS_PER_ENCRYPTION} integer ops per encryption, "
+                                                    f"{SAMPLER_ALU_ONLY_OPS} of them ALU-only, x "
                                                     f"{enc_per_index:.4f} encryptions per index; {GB300_SMS} SMs x "
-                                                    f"{SAMPLER_OPS_PER_SM_CYCLE} ops per cycle at 2070 MHz",
+                                                    f"{SAMPLER_PIPE_LANES} ALU lanes per cycle at 2070 MHz",
                                       "launches": 1, "calls_per_graph": SAMPLER_CALLS}, rows_out)
     if want("sweep"):
         # sweep (flat fp32 buffer split into cap-sized bucket launches, one graph per point): 1 KiB .. 1 GiB
