@@ -208,3 +208,24 @@ def test_split_calls_from_three_threads(g):
         assert _same(m, m_a) and _same(s, s_a), f"thread {k}"
         for r in range(n):
             assert _same(ys[r], ys_a[r]), f"thread {k} replica {r}"
+
+
+@pytest.mark.parametrize("shape", [(8, 16, 96, 28, 28), (8, 32, 34, 56, 56)])
+def test_split_halves_not_a_multiple_of_the_merge_width(g, shape):
+    """Halves of 48 and 17 channels: the merge's last CTA of each half is
+    part-full, and the second half starts inside a 32-channel group of the
+    whole call.  Every channel's statistics against the oracle, and the
+    outputs of the channels on both sides of the split."""
+    n, B, C, H, W = shape
+    assert g.syncbn_channel_parts(n, g.BF16, B, C, H, W) == 2
+    xs = _inputs(shape, 1500 + C)
+    ys, m, s = _outputs(xs, C)
+    ws = torch.empty(g.syncbn_workspace_bytes(n, B, C, H, W), dtype=torch.uint8, device="cuda")
+    g.syncbn_merge_apply(xs, ys, m, s, ws)
+    sync()
+    host = [x.view(torch.int16).cpu().numpy().view(np.uint16) for x in xs]
+    m_w, s_w = oracle.syncbn_stats(host, 1e-5)
+    m_all, s_all = m.cpu().numpy().astype(np.float64), s.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(m_all - m_w) <= 1e-5 * np.abs(m_w) + 1e-7 / s_w)
+    assert np.all(np.abs(s_all - s_w) <= 1e-5 * s_w)
+    _check_channels(xs, ys, m, s, None, None, [0, C // 2 - 1, C // 2, C - 1], f"split {shape}")
