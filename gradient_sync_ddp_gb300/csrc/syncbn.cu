@@ -25,8 +25,10 @@
 //          a CTA owns G consecutive channels (G*H*W about
 //          2K elements) and a slice of the samples; for one sample those G
 //          channels are one contiguous run, copied into shared memory by one
-//          bulk asynchronous copy, and each lane sums a contiguous range of
-//          one channel's plane there.
+//          bulk asynchronous copy (each warp streaming its own runs through
+//          two buffers, or, for runs too long for that, tiles of runs per
+//          CTA), and each lane sums a contiguous range of one channel's plane
+//          there.
 //        staged group kernel — planes shorter than a vector (1x1, 2x2):
 //          runs are copied to shared memory and reduced per channel there.
 //        element kernel — unaligned planes too long to stage (111x111).
@@ -465,6 +467,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     }
 
     bool failed = false;
+    int fail_t = 0;
     for (int t = 0; t < ntiles; ++t) {
         // thread 0 waits for the tile's copies; the others wait at the CTA barrier (no issue slots)
         bool timed_out = false;
@@ -480,6 +483,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
         }
         if (__syncthreads_or(timed_out)) {                    // also orders warp 0's plain tail stores
             failed = true;
+            fail_t = t;
             break;
         }
         const int tb = p0 + t * R, nr = min(R, p1 - tb);
@@ -501,6 +505,18 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
         __syncthreads();
         if (warp == 0 && t + 2 < ntiles) issue(t + 2);
     }
+    if (failed) {
+        // let the copies in flight (the failed tile's and the next one's) land, bounded, before the
+        // shared memory is reused
+        if (threadIdx.x == 0)
+            for (int u = fail_t; u < ntiles && u < fail_t + 2; ++u) {
+                const uint32_t pu = static_cast<uint32_t>(u >> 1) & 1u;
+                const uint64_t start = global_ns();
+                while (!mbar_try_wait(&bar[u & 1], pu) && global_ns() - start <= kCopyWaitNs) {
+                }
+            }
+        __syncthreads();
+    }
 
     // combine: smem holds [warp][m][lane] sums, then one thread per channel adds the warps' and
     // lanes' shares in a fixed order in float-float
@@ -515,6 +531,155 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     if (threadIdx.x < Gc) {
         const int c = threadIdx.x;
         const int cps = 32 >> a.tc_log2;          // channels per 32 lanes
+        const int m = c / cps;
+        const int l0 = (c % cps) << a.tc_log2;
+        const int nl = Tc;
+        FF S{0.0f, 0.0f}, Q{0.0f, 0.0f};
+        for (int w = 0; w < kWarps; ++w)
+            for (int l = l0; l < l0 + nl; ++l) {
+                S = ff_add(S, FF{red_s[(w * CPL + m) * 32 + l], 0.0f});
+                Q = ff_add(Q, FF{red_q[(w * CPL + m) * 32 + l], 0.0f});
+            }
+        a.partial[static_cast<int64_t>(c0 + c) * a.S + s] =
+            failed ? make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000))
+                   : make_float2(__fadd_rn(S.hi, S.lo), __fadd_rn(Q.hi, Q.lo));
+    }
+}
+
+// Bulk-staged kernel with a pipeline per warp, same grid, planes and lane
+// mapping as the tiled kernel above: warp w of the CTA owns runs w, w + 8,
+// ... of the CTA's slice and streams them through kBulkWarpRuns buffers of
+// its own, each completed on its own mbarrier, which every lane of the warp
+// waits on itself; a buffer is refilled as soon as its warp has summed it.
+// No CTA barrier sits inside the loop, so a warp never waits for another
+// warp's copies or sums.  Used where the warps' buffers fit in
+// kBulkWarpMaxSmem (short runs: 7x7, 14x14, 8x8 bf16); measured on
+// 8 x [32, C, H, W] bf16 (us per call, tiled -> per warp): 2048x7x7 29.0 ->
+// 28.2, 256x14x14 20.6 -> 18.4, 2048x8x8 46.7 -> 41.5, 512x7x7 15.1 -> 13.2,
+// 1024x14x14 52.3 either way; three buffers per warp were no better.  A
+// wait that runs out marks the CTA failed; the warp then lets its copies in
+// flight land (bounded) before the shared memory is reused.
+constexpr int kBulkWarpRuns = 2;
+constexpr int kBulkWarpMaxSmem = 72 * 1024;
+
+template <bool BF16, int CPL>
+__global__ void __launch_bounds__(kThreads) bn_stats_bulkw_kernel(const __grid_constant__ BnParams a) {
+    constexpr int ESZ = BF16 ? 2 : 4;
+    constexpr int kWarps = kThreads / 32;
+    constexpr int NB = kBulkWarpRuns;                         // runs in flight per warp
+    extern __shared__ __align__(128) unsigned char smem[];   // NB run buffers per warp
+    __shared__ uint64_t bar[kWarps][NB];
+    const int c0 = blockIdx.x * a.G, s = blockIdx.y;
+    const int Gc = min(a.G, a.C - c0);
+    const int HW = a.HW;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int p0, p1;
+    slice_bounds(a, s, p0, p1);
+    const uint32_t run_bytes = static_cast<uint32_t>(Gc) * HW * ESZ;
+    const int Tc = 1 << a.tc_log2;
+    const int part = lane & (Tc - 1);
+    const uint32_t e_lo = (static_cast<uint32_t>(HW) * part) >> a.tc_log2;
+    const uint32_t e_hi = (static_cast<uint32_t>(HW) * (part + 1)) >> a.tc_log2;
+    int cl[CPL];
+    float K[CPL], acc_s[CPL], acc_q[CPL];
+    pdl_wait_then_release();   // must stay the wait-then-release form: the apply reads x before its own wait
+#pragma unroll
+    for (int m = 0; m < CPL; ++m) {
+        cl[m] = (lane >> a.tc_log2) + (32 >> a.tc_log2) * m;
+        K[m] = cl[m] < Gc ? load_elem<BF16>(a.x[0], static_cast<int64_t>(c0 + cl[m]) * HW) : 0.0f;
+        acc_s[m] = 0.0f;
+        acc_q[m] = 0.0f;
+    }
+    if (lane == 0) {
+        for (int i = 0; i < NB; ++i)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bar[warp][i])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+    unsigned char* wbuf = smem + static_cast<uint32_t>(warp) * NB * a.slot_bytes;
+    const int span = p1 - p0;
+    const int nrun = span > warp ? (span - warp + kWarps - 1) / kWarps : 0;
+    auto issue = [&](int k) {                                 // lane 0: run k of this warp into buffer k % NB
+        const uint32_t pl = static_cast<uint32_t>(p0 + warp + k * kWarps);
+        const uint32_t r = fdiv(pl, a.div_batch);
+        const uint32_t bb = pl - r * static_cast<uint32_t>(a.batch);
+        const uint64_t a0 = (static_cast<uint64_t>(bb) * a.C + c0) * HW * ESZ, a1 = a0 + run_bytes;
+        const uint64_t a0al = a0 & ~uint64_t(15);
+        const uint64_t hi = min((a1 + 15) & ~uint64_t(15), a.buf_fl);
+        unsigned char* dst = wbuf + (k % NB) * a.slot_bytes;
+        const char* src = static_cast<const char*>(a.x[r]);
+        uint64_t* bp = &bar[warp][k % NB];
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bp)),
+                     "r"(static_cast<uint32_t>(hi - a0al))
+                     : "memory");
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         smem_u32(dst)),
+                     "l"(src + a0al), "r"(static_cast<uint32_t>(hi - a0al)), "r"(smem_u32(bp))
+                     : "memory");
+        for (uint64_t q = hi; q < a1; q += ESZ) {
+            if constexpr (BF16) *reinterpret_cast<unsigned short*>(dst + (q - a0al)) = *reinterpret_cast<const unsigned short*>(src + q);
+            else *reinterpret_cast<float*>(dst + (q - a0al)) = *reinterpret_cast<const float*>(src + q);
+        }
+    };
+    if (lane == 0)
+        for (int k = 0; k < NB && k < nrun; ++k) issue(k);
+    __syncwarp();
+    bool failed = false;
+    int k = 0;
+    for (; k < nrun; ++k) {
+        const uint32_t parity = static_cast<uint32_t>(k / NB) & 1u;
+        bool to = false;
+        if (!mbar_try_wait(&bar[warp][k % NB], parity)) {
+            const uint64_t start = global_ns();
+            while (!mbar_try_wait(&bar[warp][k % NB], parity)) {
+                if (global_ns() - start > kCopyWaitNs) {
+                    to = true;
+                    break;
+                }
+            }
+        }
+        if (__any_sync(0xffffffffu, to)) {
+            failed = true;
+            break;
+        }
+        __syncwarp();                                         // lane 0's plain tail stores
+        const uint32_t pl = static_cast<uint32_t>(p0 + warp + k * kWarps);
+        const uint32_t r = fdiv(pl, a.div_batch);
+        const uint32_t bb = pl - r * static_cast<uint32_t>(a.batch);
+        const uint32_t pre = static_cast<uint32_t>(((static_cast<uint64_t>(bb) * a.C + c0) * HW * ESZ) & 15u);
+        const unsigned char* run = wbuf + (k % NB) * a.slot_bytes;
+#pragma unroll
+        for (int m = 0; m < CPL; ++m) {
+            if (cl[m] < Gc)
+                sum_range<BF16>(run, pre + (static_cast<uint32_t>(cl[m]) * HW + e_lo) * ESZ, e_hi - e_lo, K[m],
+                                a.vec_reads != 0, acc_s[m], acc_q[m]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && k + NB < nrun) issue(k + NB);
+        __syncwarp();
+    }
+    if (failed) {                                             // let this warp's copies in flight land (bounded)
+        for (int j = k; j < nrun && j < k + NB; ++j) {
+            const uint32_t parity = static_cast<uint32_t>(j / NB) & 1u;
+            const uint64_t start = global_ns();
+            while (!mbar_try_wait(&bar[warp][j % NB], parity) && global_ns() - start <= kCopyWaitNs) {
+            }
+        }
+    }
+    failed = __syncthreads_or(failed);
+    float* red_s = reinterpret_cast<float*>(smem);
+    float* red_q = red_s + kWarps * CPL * 32;
+#pragma unroll
+    for (int m = 0; m < CPL; ++m) {
+        red_s[(warp * CPL + m) * 32 + lane] = acc_s[m];
+        red_q[(warp * CPL + m) * 32 + lane] = acc_q[m];
+    }
+    __syncthreads();
+    if (threadIdx.x < Gc) {
+        const int c = threadIdx.x;
+        const int cps = 32 >> a.tc_log2;
         const int m = c / cps;
         const int l0 = (c % cps) << a.tc_log2;
         const int nl = Tc;
@@ -902,7 +1067,17 @@ int launch_bulk(int cpl, dim3 grid, int smem, cudaStream_t s, const BnParams& p)
     }
 }
 
-enum StatsKind { kPlaneVec, kPlaneScalar, kBulk, kStaged };
+template <bool BF16>
+int launch_bulkw(int cpl, dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
+    switch (cpl) {
+        case 1: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 1>, grid, smem, s, p);
+        case 2: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 2>, grid, smem, s, p);
+        case 4: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 4>, grid, smem, s, p);
+        default: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 8>, grid, smem, s, p);
+    }
+}
+
+enum StatsKind { kPlaneVec, kPlaneScalar, kBulk, kBulkWarp, kStaged };
 
 struct StatsPlan {
     StatsKind kind;
@@ -1007,7 +1182,13 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
         // other loop (on 7x7 planes, per-lane alignment tests cost 28.3 -> 32.7 us)
         sp.vec_reads = esz == 2 && HW % W == 0 && (HW / W) % (1 << tl) == 0;
         const int red = kThreads * sp.cpl * 2 * static_cast<int>(sizeof(float));
-        sp.smem = 2 * sp.R * slot > red ? 2 * sp.R * slot : red;
+        const int warp_bufs = (kThreads / 32) * kBulkWarpRuns * slot;
+        if (warp_bufs <= kBulkWarpMaxSmem) {
+            sp.kind = kBulkWarp;
+            sp.smem = warp_bufs > red ? warp_bufs : red;
+        } else {
+            sp.smem = 2 * sp.R * slot > red ? 2 * sp.R * slot : red;
+        }
         sp.S = bulk_slices((C + G - 1) / G, P, C, sp.smem, sp.cpl);
     } else if (sp.kind == kStaged) {
         sp.G = G;
@@ -1161,11 +1342,13 @@ SideStream* side_stream(cudaStream_t caller) {
 // [p.c_base, p.c_end), on stream s.
 int launch_sequence(BnParams p, const StatsPlan& sp, bool bf16_in, bool bf16_out, bool nc, cudaStream_t s) {
     int st;
-    if (sp.kind == kBulk || sp.kind == kStaged) {
+    if (sp.kind == kBulk || sp.kind == kBulkWarp || sp.kind == kStaged) {
         p.div_unit = make_fastdiv(static_cast<uint32_t>(sp.slot_bytes / 16));
         const dim3 grid(static_cast<unsigned>((p.C + sp.G - 1) / sp.G), static_cast<unsigned>(sp.S));
         if (sp.kind == kBulk)
             st = bf16_in ? launch_bulk<true>(sp.cpl, grid, sp.smem, s, p) : launch_bulk<false>(sp.cpl, grid, sp.smem, s, p);
+        else if (sp.kind == kBulkWarp)
+            st = bf16_in ? launch_bulkw<true>(sp.cpl, grid, sp.smem, s, p) : launch_bulkw<false>(sp.cpl, grid, sp.smem, s, p);
         else
             st = bf16_in ? launch_pdl(bn_stats_group_kernel<true>, grid, kThreads, s, p)
                          : launch_pdl(bn_stats_group_kernel<false>, grid, kThreads, s, p);
