@@ -388,8 +388,8 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
     constexpr int kWarps = kThreads / 32;
     extern __shared__ __align__(128) unsigned char smem[];   // two tile buffers of R * slot_bytes
     __shared__ uint64_t bar[2];
-    const int c0 = blockIdx.x * a.G, s = blockIdx.y;
-    const int Gc = min(a.G, a.C - c0);
+    const int c0 = a.c_base + blockIdx.x * a.G, s = blockIdx.y;
+    const int Gc = min(a.G, a.c_end - c0);
     const int HW = a.HW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int p0, p1;
@@ -569,8 +569,8 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulkw_kernel(const __grid_c
     constexpr int NB = kBulkWarpRuns;                         // runs in flight per warp
     extern __shared__ __align__(128) unsigned char smem[];   // NB run buffers per warp
     __shared__ uint64_t bar[kWarps][NB];
-    const int c0 = blockIdx.x * a.G, s = blockIdx.y;
-    const int Gc = min(a.G, a.C - c0);
+    const int c0 = a.c_base + blockIdx.x * a.G, s = blockIdx.y;
+    const int Gc = min(a.G, a.c_end - c0);
     const int HW = a.HW;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int p0, p1;
@@ -901,7 +901,10 @@ __device__ __forceinline__ uint32_t channel_of(uint32_t e, const BnParams& a) {
 //            sample, so the thread finds its channels and packs their
 //            coefficients once, before its loop;
 //        4 = as 0, over the channels [c_base, c_end) only: the launch's
-//            vectors are those channels' runs in each sample.
+//            vectors are those channels' runs in each sample;
+//        5 = as 3 over the channels [c_base, c_end) only (the part's run in
+//            a sample a whole number of vectors, the grid stride a whole
+//            number of such runs).
 template <bool BF16_IN, bool BF16_OUT, int CMODE, bool NC>
 __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constant__ BnParams a) {
     // replicas and vectors are visited in the reverse of the statistics pass's order (its last CTAs
@@ -914,9 +917,10 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
     const uint32_t nvec = E / 8;
     const uint32_t stride = gridDim.x * kThreads;
     const uint32_t gtid = blockIdx.x * kThreads + threadIdx.x;
-    // vector index within the replica of this launch's vector vr (mode 4: a part of the channels)
+    // vector index within the replica of this launch's vector vr (modes 4 and 5: a part of the
+    // channels)
     auto full_vec = [&](uint32_t vr) -> uint32_t {
-        if constexpr (CMODE == 4) {
+        if constexpr (CMODE == 4 || CMODE == 5) {
             const uint32_t b = fdiv(vr, a.div_vp);
             return b * a.vs_full + a.v_base + (vr - b * static_cast<uint32_t>(a.div_vp.d));
         }
@@ -940,14 +944,17 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
     // in the stream had completed; the coefficients are read after the wait
     if (gtid < nvec) load4(gtid);
     pdl_enter();
-    // mode 3: the coefficient pairs of this thread's element positions (fixed for all its vectors)
+    // modes 3 and 5: the coefficient pairs of this thread's element positions (fixed for all its
+    // vectors)
     uint64_t M2[4], S2[4], T2[4];
-    if constexpr (CMODE == 3) {
+    if constexpr (CMODE == 3 || CMODE == 5) {
         float4 kA = make_float4(0.0f, 0.0f, 0.0f, 0.0f), kB = kA;
         uint32_t eb = 8;
         if (gtid < nvec) {
             const uint32_t vr = nvec - 1 - gtid;
-            const uint32_t e0 = (vr - fdiv(vr, a.div_vs8) * static_cast<uint32_t>(a.div_vs8.d)) * 8;   // in the sample
+            uint32_t e0;                                    // element offset in the sample
+            if constexpr (CMODE == 3) e0 = (vr - fdiv(vr, a.div_vs8) * static_cast<uint32_t>(a.div_vs8.d)) * 8;
+            else e0 = (a.v_base + vr - fdiv(vr, a.div_vp) * static_cast<uint32_t>(a.div_vp.d)) * 8;
             const uint32_t cA = fdiv(e0, a.div_hw);
             eb = (cA + 1) * static_cast<uint32_t>(a.HW) - e0;
             kA = __ldg(a.coef + cA);
@@ -988,7 +995,7 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
                 for (int j = 0; j < 4; ++j)
                     yv2[j] = normalize2(xv[j], static_cast<uint32_t>(2 * j) < cross ? k0 : k1,
                                         static_cast<uint32_t>(2 * j + 1) < cross ? k0 : k1);
-            } else if constexpr (CMODE == 3) {
+            } else if constexpr (CMODE == 3 || CMODE == 5) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) yv2[j] = f2_fma(f2_sub(xv[j], M2[j]), S2[j], T2[j]);
             } else {
@@ -1084,6 +1091,7 @@ struct StatsPlan {
     int G, S, R, slot_bytes;
     int smem;           // bulk kernel: dynamic shared bytes (two tile buffers)
     int tc_log2, cpl;   // bulk kernel: log2 of the lanes per channel, channels per lane
+    bool split;         // the call runs as two channel halves on two streams
     bool vec_reads;     // bulk kernel: every lane's range starts on a 16-byte boundary of its run
 };
 
@@ -1135,6 +1143,28 @@ int slices_for(int n_groups, int P, int C) {
 int slot_bytes_for(int G, int HW, int esz) {
     return static_cast<int>((static_cast<int64_t>(G) * HW * esz + 14 + 15) / 16 * 16);
 }
+
+// Whether a call runs as two channel halves on two streams (the first half's
+// statistics, merge and apply on the caller's stream, the second half's on a
+// side stream), so that each half's launches fill the other's gaps: the
+// three launches of a call depend on each other, and between them the
+// memory idles through a grid's drain, the merge and the next ramp.  Taken
+// where the input over all replicas is large enough and the channels split
+// evenly into whole statistics units: aligned planes with the plane kernel
+// (even C, halves of at least 16 channels, 16 MiB), and unaligned planes
+// with the per-warp bulk-staged kernel (halves of whole channel groups whose
+// run in a sample is a whole number of 16-byte vectors, 32 MiB).  Measured
+// on 8 x [32, C, H, W] bf16 with inputs rotated past L2 (us per call, one
+// sequence -> two halves): 64x56x56 46.1 -> 45.5, 256x56x56 188.5 -> 181.9,
+// 512x28x28 95.9 -> 92.0, 64x28x28 22.9 -> 19.7, 2048x7x7 27.9 -> 25.4,
+// 1024x14x14 52.3 -> 49.3; 256x14x14 (26 MB) gained nothing, and short
+// aligned planes on the bulk kernel lost (2048x8x8 41.1 -> 43.6, 8192x4x4
+// 41.0 -> 43.0).  Both halves
+// use one slice count, fitted to a half, so the sums, and every output bit,
+// are those of the call run as one sequence with that count.
+constexpr int64_t kSplitMinBytes = int64_t(16) << 20;       // x over all replicas, plane statistics
+constexpr int64_t kSplitBulkMinBytes = int64_t(32) << 20;   // x over all replicas, bulk-staged statistics
+constexpr int kSplitMinChannels = 16;                         // per half
 
 // Aligned planes of at least kPlaneMinVecs vectors: plane kernel with
 // 16-byte loads.  A warp reads 64-vector chunks of one plane, so shorter
@@ -1189,7 +1219,10 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
         } else {
             sp.smem = 2 * sp.R * slot > red ? 2 * sp.R * slot : red;
         }
-        sp.S = bulk_slices((C + G - 1) / G, P, C, sp.smem, sp.cpl);
+        const int64_t bytes = static_cast<int64_t>(n) * batch * C * HW * esz;
+        sp.split = sp.kind == kBulkWarp && HW % W != 0 && C % 2 == 0 && C / 2 >= kSplitMinChannels &&
+                   (C / 2) % G == 0 && (static_cast<int64_t>(C / 2) * HW) % 8 == 0 && bytes >= kSplitBulkMinBytes;
+        sp.S = bulk_slices(((sp.split ? C / 2 : C) + G - 1) / G, P, C, sp.smem, sp.cpl);
     } else if (sp.kind == kStaged) {
         sp.G = G;
         sp.slot_bytes = slot;
@@ -1209,6 +1242,8 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
             if (S > kMaxPartials / C) S = kMaxPartials / C;
             if (S < 1) S = 1;
             sp.S = static_cast<int>(S);
+            sp.split = HW % 8 == 0 && C % 2 == 0 && C / 2 >= kSplitMinChannels &&
+                       static_cast<int64_t>(n) * batch * C * HW * esz >= kSplitMinBytes;
         }
     }
     return sp;
@@ -1268,26 +1303,12 @@ int launch_apply(const BnParams& p, int cmode, bool nc, dim3 grid, cudaStream_t 
     if (cmode == 1) return launch_apply_mode<BF16_IN, BF16_OUT, 1>(p, nc, grid, s);
     if (cmode == 3) return launch_apply_mode<BF16_IN, BF16_OUT, 3>(p, nc, grid, s);
     if (cmode == 4) return launch_apply_mode<BF16_IN, BF16_OUT, 4>(p, nc, grid, s);
+    if (cmode == 5) return launch_apply_mode<BF16_IN, BF16_OUT, 5>(p, nc, grid, s);
     return launch_apply_mode<BF16_IN, BF16_OUT, 2>(p, nc, grid, s);
 }
 
-// Whether a call runs as two channel halves on two streams: aligned planes
-// (plane statistics, apply mode 0), an even channel count and an input large
-// enough that three short launches leave the memory idle between them.
-// Measured on 8 x [32, C, H, W] bf16 with inputs rotated past L2 (us per
-// call, one sequence -> two halves): 64x56x56 46.1 -> 45.5, 256x56x56
-// 188.5 -> 181.9, 512x28x28 95.9 -> 92.0, 64x28x28 22.9 -> 19.7; as two
-// independent half-size calls, 2048x7x7 (bulk statistics) gained nothing.
-// Both halves use one slice count, fitted to the half's grid, so the sums,
-// and every output bit, are those of the call run as one sequence with
-// that count.
-constexpr int64_t kSplitMinBytes = int64_t(16) << 20;   // x over all replicas
-constexpr int kSplitMinChannels = 16;                     // per half
 
-bool split_channels(const StatsPlan& sp, int n, int batch, int C, int HW, int esz) {
-    return sp.kind == kPlaneVec && HW % 8 == 0 && C % 2 == 0 && C / 2 >= kSplitMinChannels &&
-           static_cast<int64_t>(n) * batch * C * HW * esz >= kSplitMinBytes;
-}
+bool split_channels(const StatsPlan& sp) { return sp.split; }
 
 // A side stream and its fork and join events, one per host thread and
 // device, created on the thread's first split call outside stream capture
@@ -1344,7 +1365,7 @@ int launch_sequence(BnParams p, const StatsPlan& sp, bool bf16_in, bool bf16_out
     int st;
     if (sp.kind == kBulk || sp.kind == kBulkWarp || sp.kind == kStaged) {
         p.div_unit = make_fastdiv(static_cast<uint32_t>(sp.slot_bytes / 16));
-        const dim3 grid(static_cast<unsigned>((p.C + sp.G - 1) / sp.G), static_cast<unsigned>(sp.S));
+        const dim3 grid(static_cast<unsigned>((p.c_end - p.c_base + sp.G - 1) / sp.G), static_cast<unsigned>(sp.S));
         if (sp.kind == kBulk)
             st = bf16_in ? launch_bulk<true>(sp.cpl, grid, sp.smem, s, p) : launch_bulk<false>(sp.cpl, grid, sp.smem, s, p);
         else if (sp.kind == kBulkWarp)
@@ -1384,10 +1405,12 @@ int launch_sequence(BnParams p, const StatsPlan& sp, bool bf16_in, bool bf16_out
     if (gx > cap) gx = cap;
     if (gx < 1) gx = 1;
     int cmode = (p.HW % 8) == 0 ? (p.parted ? 4 : 0) : (p.HW >= 8 ? 1 : 2);
-    if (cmode == 1 && (static_cast<int64_t>(p.C) * p.HW) % 8 == 0) {
-        // mode 3: a grid stride (gx*kThreads vectors) that is a whole number of samples, with gx the
-        // multiple of the smallest such count nearest to the size chosen above
-        const int64_t vs8 = static_cast<int64_t>(p.C) * p.HW / 8;
+    const int64_t run_elems = static_cast<int64_t>(p.c_end - p.c_base) * p.HW;   // a sample's run of this launch
+    if (cmode == 1 && run_elems % 8 == 0) {
+        // mode 3 (5 for a part): a grid stride (gx*kThreads vectors) that is a whole number of the
+        // launch's runs, with gx the multiple of the smallest such count nearest to the size
+        // chosen above (a part is split off only where its run is a whole number of vectors)
+        const int64_t vs8 = run_elems / 8;
         int64_t gcd = kThreads, tmp = vs8;
         while (tmp != 0) {                                  // gcd(kThreads, vs8)
             const int64_t q = gcd % tmp;
@@ -1399,10 +1422,11 @@ int launch_sequence(BnParams p, const StatsPlan& sp, bool bf16_in, bool bf16_out
         if (g3 < m0) g3 = m0;
         if (g3 <= 2 * gx + m0 && g3 * kThreads <= (int64_t(1) << 31) / 4) {
             gx = g3;
-            cmode = 3;
+            cmode = p.parted ? 5 : 3;
             p.div_vs8 = make_fastdiv(static_cast<uint32_t>(vs8));
         }
     }
+    if (p.parted && cmode != 4 && cmode != 5) return DDP_ERR_UNSUPPORTED;   // excluded by the split rule
     const dim3 agrid(static_cast<unsigned>(gx), static_cast<unsigned>(p.n));
     if (bf16_in) return bf16_out ? launch_apply<true, true>(p, cmode, nc, agrid, s) : launch_apply<true, false>(p, cmode, nc, agrid, s);
     return bf16_out ? launch_apply<false, true>(p, cmode, nc, agrid, s) : launch_apply<false, false>(p, cmode, nc, agrid, s);
@@ -1425,7 +1449,7 @@ extern "C" int syncbn_channel_parts(int32_t n_replicas, int32_t in_dtype, int32_
         return DDP_ERR_INVALID_ARG;
     const int esz = in_dtype == DDP_BF16 ? 2 : 4;
     const StatsPlan sp = plan_stats(n_replicas, batch, C, H * W, esz);
-    return split_channels(sp, n_replicas, batch, C, H * W, esz) ? 2 : 1;
+    return split_channels(sp) ? 2 : 1;
 }
 
 extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int32_t in_dtype,
@@ -1466,7 +1490,7 @@ extern "C" int syncbn_merge_apply(const void* const* x, int32_t n_replicas, int3
     const bool bf16_in = in_dtype == DDP_BF16;
     const int esz = bf16_in ? 2 : 4;
     StatsPlan sp = plan_stats(n_replicas, batch, C, H * W, esz);
-    const bool split = split_channels(sp, n_replicas, batch, C, H * W, esz);
+    const bool split = split_channels(sp);
     int st;
     if (sp.kind == kPlaneVec) {
         // the plan's slice count sizes the workspace; the launch may take fewer to end on a full wave

@@ -312,20 +312,30 @@ def test_mean_multi_rejects(g):
 def test_syncbn_channel_parts(g):
     """Which SyncBN calls run as two channel halves on two streams: aligned
     planes with the plane statistics kernel (H*W a multiple of 8 and, for
-    bf16, at least 16 vectors), an even C of at least 32 and 16 MiB of input
-    over all replicas.  The planner decides on the host, no GPU needed."""
+    bf16, at least 16 vectors; even C, halves of at least 16 channels, 16 MiB
+    of input over all replicas), and calls with the per-warp bulk-staged
+    statistics (halves of whole channel groups whose run in a sample is a
+    whole number of 16-byte vectors, 32 MiB, unaligned planes only).  The planner decides on the
+    host, no GPU needed."""
     bf16, f32 = g.BF16, g.F32
     assert g.syncbn_channel_parts(8, bf16, 32, 64, 56, 56) == 2
     assert g.syncbn_channel_parts(8, bf16, 32, 256, 56, 56) == 2
     assert g.syncbn_channel_parts(8, bf16, 32, 512, 28, 28) == 2
-    assert g.syncbn_channel_parts(8, bf16, 32, 2048, 7, 7) == 1       # unaligned: bulk-staged statistics
-    assert g.syncbn_channel_parts(8, bf16, 32, 2048, 8, 8) == 1       # 8 vectors per plane: bulk-staged
+    assert g.syncbn_channel_parts(8, bf16, 32, 2048, 7, 7) == 2       # per-warp bulk-staged statistics
+    assert g.syncbn_channel_parts(8, f32, 32, 2048, 7, 7) == 1        # fp32 runs: tiled bulk kernel
+    assert g.syncbn_channel_parts(8, bf16, 32, 2047, 7, 7) == 1       # odd C
+    assert g.syncbn_channel_parts(8, bf16, 32, 512, 7, 7) == 1        # 12.8 MB: under 32 MiB
+    assert g.syncbn_channel_parts(8, bf16, 32, 1024, 14, 14) == 2
+    assert g.syncbn_channel_parts(8, bf16, 32, 256, 14, 14) == 1      # 26 MB
+    assert g.syncbn_channel_parts(8, bf16, 32, 1024, 17, 17) == 2     # groups of 4 channels, runs of 1156
+    assert g.syncbn_channel_parts(8, bf16, 32, 1032, 17, 17) == 1     # a half's run of 516*289 elements
+    assert g.syncbn_channel_parts(8, bf16, 32, 2048, 8, 8) == 1       # 8 vectors per plane: bulk-staged, aligned
     assert g.syncbn_channel_parts(8, f32, 32, 2048, 8, 8) == 2        # fp32: plane kernel, 16 vectors
     assert g.syncbn_channel_parts(8, bf16, 32, 65, 56, 56) == 1       # odd C
     assert g.syncbn_channel_parts(8, bf16, 32, 30, 56, 56) == 1       # 15 channels per half
     assert g.syncbn_channel_parts(8, bf16, 32, 32, 56, 56) == 2       # 16 per half, 51 MB
     assert g.syncbn_channel_parts(2, bf16, 32, 32, 56, 56) == 1       # 12.8 MB: under 16 MiB
-    assert g.syncbn_channel_parts(8, bf16, 32, 64, 28, 29) == 1       # H*W = 812: not a multiple of 8
+    assert g.syncbn_channel_parts(8, bf16, 32, 64, 28, 29) == 1       # H*W = 812: bulk-staged, 26.6 MB
     for bad in [(0, bf16, 32, 64, 56, 56), (17, bf16, 32, 64, 56, 56), (8, 7, 32, 64, 56, 56),
                 (8, bf16, 0, 64, 56, 56), (8, bf16, 32, 64, 0, 56)]:
         with pytest.raises(RuntimeError):

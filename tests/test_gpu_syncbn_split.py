@@ -1,11 +1,12 @@
 """SyncBN calls that run as two channel halves on two streams.
 
 Calls on aligned planes that take the plane statistics kernel (H*W a
-multiple of 8), with an even C of at least 32 and at least 16 MiB of input
-over all replicas, run the statistics, merge and apply of channels [0, C/2)
-on the caller's stream and those of [C/2, C) on a side stream that the
-library keeps per host thread and device, joined back before the call
-returns.  Both halves use one slice count, so the split call and the call
+multiple of 8; an even C of at least 32 and at least 16 MiB of input over
+all replicas), and calls on unaligned planes that take the per-warp
+bulk-staged statistics (halves of whole channel groups, 32 MiB), run the
+statistics, merge and apply of channels [0, C/2) on the caller's stream and
+those of [C/2, C) on a side stream that the library keeps per host thread
+and device, joined back before the call returns.  Both halves use one slice count, so the split call and the call
 run as one sequence give the same bits: a thread's first call made inside a
 stream capture, which finds no side stream yet, runs as one sequence, and
 its replay must equal the split call bit for bit.  The statistics are
@@ -229,3 +230,71 @@ def test_split_halves_not_a_multiple_of_the_merge_width(g, shape):
     assert np.all(np.abs(m_all - m_w) <= 1e-5 * np.abs(m_w) + 1e-7 / s_w)
     assert np.all(np.abs(s_all - s_w) <= 1e-5 * s_w)
     _check_channels(xs, ys, m, s, None, None, [0, C // 2 - 1, C // 2, C - 1], f"split {shape}")
+
+
+@pytest.mark.parametrize("shape", [(8, 32, 2048, 7, 7), (8, 16, 1024, 14, 14), (8, 16, 1024, 17, 17)])
+def test_bulk_statistics_split_matches_oracle(g, shape):
+    """Calls whose statistics take the per-warp bulk-staged kernel split into
+    halves of whole channel groups (unaligned 7x7, 14x14 and 17x17 planes;
+    the apply's mode 5).  Every channel's statistics against the oracle, and
+    the outputs on both sides of the split."""
+    n, B, C, H, W = shape
+    assert g.syncbn_channel_parts(n, g.BF16, B, C, H, W) == 2
+    xs = _inputs(shape, 1600 + H)
+    gamma = workloads.device_normal((C,), 1.0, 0.1, 1700)
+    beta = workloads.device_normal((C,), 0.0, 0.1, 1701)
+    ys, m, s = _outputs(xs, C)
+    ws = torch.empty(g.syncbn_workspace_bytes(n, B, C, H, W), dtype=torch.uint8, device="cuda")
+    g.syncbn_merge_apply(xs, ys, m, s, ws, 1e-5, gamma, beta)
+    sync()
+    host = [x.view(torch.int16).cpu().numpy().view(np.uint16) for x in xs]
+    m_w, s_w = oracle.syncbn_stats(host, 1e-5)
+    m_all, s_all = m.cpu().numpy().astype(np.float64), s.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(m_all - m_w) <= 1e-5 * np.abs(m_w) + 1e-7 / s_w)
+    assert np.all(np.abs(s_all - s_w) <= 1e-5 * s_w)
+    _check_channels(xs, ys, m, s, gamma, beta, [0, 1, C // 2 - 1, C // 2, C // 2 + 1, C - 1], f"bulk split {shape}")
+
+
+def test_bulk_split_in_graph_and_unsplit_capture_give_the_same_bits(g):
+    """7x7 planes: the eager split call, its graph replay, and a new thread's
+    first call made inside a capture (one sequence on the capturing stream)
+    agree bit for bit."""
+    shape = (8, 32, 2048, 7, 7)
+    n, B, C, H, W = shape
+    xs = _inputs(shape, 1800)
+    ws = torch.empty(g.syncbn_workspace_bytes(n, B, C, H, W), dtype=torch.uint8, device="cuda")
+    ys_e, m_e, s_e = _outputs(xs, C)
+    g.syncbn_merge_apply(xs, ys_e, m_e, s_e, ws)
+    sync()
+    ys_g, m_g, s_g = _outputs(xs, C)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        g.syncbn_merge_apply(xs, ys_g, m_g, s_g, ws)
+    graph.replay()
+    sync()
+    ys_t, m_t, s_t = _outputs(xs, C)
+    ws2 = torch.empty_like(ws)
+    errors = []
+
+    def worker():
+        try:
+            torch.cuda.set_device(0)
+            st = torch.cuda.Stream()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=st):
+                g.syncbn_merge_apply(xs, ys_t, m_t, s_t, ws2)
+            gr.replay()
+            torch.cuda.synchronize()
+        except Exception as e:         # reported by the main thread
+            errors.append(repr(e))
+
+    t = threading.Thread(target=worker)
+    t.start()
+    t.join(timeout=300)
+    assert not errors, errors
+    for m, s, ys, what in ((m_g, s_g, ys_g, "graph"), (m_t, s_t, ys_t, "unsplit capture")):
+        assert _same(m, m_e) and _same(s, s_e), what
+        for r in range(n):
+            assert _same(ys[r], ys_e[r]), f"{what} replica {r}"
