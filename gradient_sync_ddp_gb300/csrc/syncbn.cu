@@ -6,9 +6,9 @@
 // AI_Infra notes "1.DataParallel / DDP" §4.3: the synced statistics are those
 // of the whole global batch (one extra all-reduce per BN layer).
 //
-// Three launches on the caller's stream (large aligned-plane calls: three for
-// each channel half, the second half on a side stream joined back before the
-// call returns):
+// Three launches on the caller's stream (large calls: three for each channel
+// half, the second half on a side stream joined back before the call
+// returns):
 //   1. stats  — per-channel partial sums over slices of the N*batch samples.
 //      The sums are shifted by K_c, the channel's first element (replica 0,
 //      sample 0): d = x − K_c, and Σd, Σd² are accumulated, so Q/M − mean²

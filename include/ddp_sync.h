@@ -436,7 +436,8 @@ int syncbn_channel_parts(int32_t n_replicas, int32_t in_dtype, int32_t batch, in
  *                kernels may overlap on the GPU (different streams without
  *                ordering) need different workspaces, or they race on the
  *                partial sums
- * Streams: large inputs with H*W a multiple of 8 and an even C run as two
+ * Streams: large inputs whose channels split evenly into the statistics
+ * kernels' units (an even C; see syncbn_channel_parts) run as two
  * channel halves, the second on a side stream that the library keeps per
  * host thread and device (created on the thread's first such call made
  * outside stream capture; a call that finds none while its stream captures
