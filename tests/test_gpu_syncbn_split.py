@@ -232,18 +232,22 @@ def test_split_halves_not_a_multiple_of_the_merge_width(g, shape):
     _check_channels(xs, ys, m, s, None, None, [0, C // 2 - 1, C // 2, C - 1], f"split {shape}")
 
 
-@pytest.mark.parametrize("shape", [(8, 32, 2048, 7, 7), (8, 16, 1024, 14, 14), (8, 16, 1024, 17, 17)])
-def test_bulk_statistics_split_matches_oracle(g, shape):
+@pytest.mark.parametrize("shape,out_dtype", [((8, 32, 2048, 7, 7), torch.bfloat16), ((8, 32, 2048, 7, 7), torch.float32),
+                                             ((8, 16, 1024, 14, 14), torch.bfloat16),
+                                             ((8, 16, 1024, 17, 17), torch.bfloat16)])
+def test_bulk_statistics_split_matches_oracle(g, shape, out_dtype):
     """Calls whose statistics take the per-warp bulk-staged kernel split into
     halves of whole channel groups (unaligned 7x7, 14x14 and 17x17 planes;
-    the apply's mode 5).  Every channel's statistics against the oracle, and
-    the outputs on both sides of the split."""
+    the apply's mode 5, with bf16 and fp32 outputs).  Every channel's
+    statistics against the oracle, and the outputs on both sides of the
+    split."""
     n, B, C, H, W = shape
     assert g.syncbn_channel_parts(n, g.BF16, B, C, H, W) == 2
     xs = _inputs(shape, 1600 + H)
     gamma = workloads.device_normal((C,), 1.0, 0.1, 1700)
     beta = workloads.device_normal((C,), 0.0, 0.1, 1701)
-    ys, m, s = _outputs(xs, C)
+    ys = [torch.full(x.shape, float("nan"), dtype=out_dtype, device="cuda") for x in xs]
+    m, s = torch.full((C,), float("nan"), device="cuda"), torch.full((C,), float("nan"), device="cuda")
     ws = torch.empty(g.syncbn_workspace_bytes(n, B, C, H, W), dtype=torch.uint8, device="cuda")
     g.syncbn_merge_apply(xs, ys, m, s, ws, 1e-5, gamma, beta)
     sync()
