@@ -562,10 +562,18 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
 constexpr int kBulkWarpRuns = 2;
 constexpr int kBulkWarpMaxSmem = 72 * 1024;
 
+// Threads per CTA of the per-warp kernel: 4 warps where a lane holds one or
+// two channels (twice the CTAs, each with a quarter of the SM's run
+// buffers: split 7x7 calls 25.7 -> 24.8 us, 1024x14x14 49.3 -> 48.5), 8
+// where it holds four or eight (short aligned planes: 8x8 41.2 against
+// 42.1 us with 4 warps).
+__host__ __device__ constexpr int bulkw_threads(int cpl) { return cpl >= 4 ? 256 : 128; }
+
 template <bool BF16, int CPL>
-__global__ void __launch_bounds__(kThreads) bn_stats_bulkw_kernel(const __grid_constant__ BnParams a) {
+__global__ void __launch_bounds__(bulkw_threads(CPL)) bn_stats_bulkw_kernel(const __grid_constant__ BnParams a) {
     constexpr int ESZ = BF16 ? 2 : 4;
-    constexpr int kWarps = kThreads / 32;
+    constexpr int kT = bulkw_threads(CPL);
+    constexpr int kWarps = kT / 32;
     constexpr int NB = kBulkWarpRuns;                         // runs in flight per warp
     extern __shared__ __align__(128) unsigned char smem[];   // NB run buffers per warp
     __shared__ uint64_t bar[kWarps][NB];
@@ -677,8 +685,7 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulkw_kernel(const __grid_c
         red_q[(warp * CPL + m) * 32 + lane] = acc_q[m];
     }
     __syncthreads();
-    if (threadIdx.x < Gc) {
-        const int c = threadIdx.x;
+    for (int c = threadIdx.x; c < Gc; c += kT) {
         const int cps = 32 >> a.tc_log2;
         const int m = c / cps;
         const int l0 = (c % cps) << a.tc_log2;
@@ -1031,7 +1038,8 @@ __global__ void __launch_bounds__(kThreads) bn_apply_kernel(const __grid_constan
 
 // Launch with `smem` bytes of dynamic shared memory and programmatic stream
 // serialisation; the opt-in above 48 KiB is set once per kernel and device.
-int launch_pdl_smem(void (*kernel)(BnParams), dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
+int launch_pdl_smem(void (*kernel)(BnParams), dim3 grid, int smem, cudaStream_t s, const BnParams& p,
+                    int block = kThreads) {
     static std::mutex mu;
     static std::map<std::pair<const void*, int>, int> granted;   // (kernel, device) -> bytes allowed
     if (smem > 48 * 1024) {
@@ -1050,7 +1058,7 @@ int launch_pdl_smem(void (*kernel)(BnParams), dim3 grid, int smem, cudaStream_t 
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(static_cast<unsigned>(kThreads));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1077,10 +1085,10 @@ int launch_bulk(int cpl, dim3 grid, int smem, cudaStream_t s, const BnParams& p)
 template <bool BF16>
 int launch_bulkw(int cpl, dim3 grid, int smem, cudaStream_t s, const BnParams& p) {
     switch (cpl) {
-        case 1: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 1>, grid, smem, s, p);
-        case 2: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 2>, grid, smem, s, p);
-        case 4: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 4>, grid, smem, s, p);
-        default: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 8>, grid, smem, s, p);
+        case 1: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 1>, grid, smem, s, p, bulkw_threads(1));
+        case 2: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 2>, grid, smem, s, p, bulkw_threads(2));
+        case 4: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 4>, grid, smem, s, p, bulkw_threads(4));
+        default: return launch_pdl_smem(bn_stats_bulkw_kernel<BF16, 8>, grid, smem, s, p, bulkw_threads(8));
     }
 }
 
@@ -1101,11 +1109,11 @@ struct StatsPlan {
 // correctness) depends on it.
 constexpr int kWaveSms = 152;
 
-int bulk_slices(int n_groups, int P, int C, int smem, int cpl) {
+int bulk_slices(int n_groups, int P, int C, int smem, int cpl, int ctas_per_256) {
     int per_sm = (227 * 1024) / (smem + 1024);              // shared memory per SM, 1 KiB reserved per CTA
     // registers: 6 CTAs of 256 threads with one channel per lane (40 registers), 5 with two (48),
-    // 4 with four or eight (59-64)
-    const int reg_cap = cpl >= 4 ? 4 : (cpl == 2 ? 5 : 6);
+    // 4 with four or eight (59-64); twice as many CTAs of 128 threads
+    const int reg_cap = (cpl >= 4 ? 4 : (cpl == 2 ? 5 : 6)) * ctas_per_256;
     if (per_sm > reg_cap) per_sm = reg_cap;
     if (per_sm < 1) per_sm = 1;
     int64_t S = static_cast<int64_t>(kWaveSms) * per_sm / n_groups;
@@ -1212,17 +1220,20 @@ StatsPlan plan_stats(int n, int batch, int C, int HW, int esz) {
         // other loop (on 7x7 planes, per-lane alignment tests cost 28.3 -> 32.7 us)
         sp.vec_reads = esz == 2 && HW % W == 0 && (HW / W) % (1 << tl) == 0;
         const int red = kThreads * sp.cpl * 2 * static_cast<int>(sizeof(float));
-        const int warp_bufs = (kThreads / 32) * kBulkWarpRuns * slot;
-        if (warp_bufs <= kBulkWarpMaxSmem) {
+        if ((kThreads / 32) * kBulkWarpRuns * slot <= kBulkWarpMaxSmem) {
             sp.kind = kBulkWarp;
-            sp.smem = warp_bufs > red ? warp_bufs : red;
+            const int bt = bulkw_threads(sp.cpl);
+            const int warp_bufs = (bt / 32) * kBulkWarpRuns * slot;
+            const int redw = bt * sp.cpl * 2 * static_cast<int>(sizeof(float));
+            sp.smem = warp_bufs > redw ? warp_bufs : redw;
         } else {
             sp.smem = 2 * sp.R * slot > red ? 2 * sp.R * slot : red;
         }
         const int64_t bytes = static_cast<int64_t>(n) * batch * C * HW * esz;
         sp.split = sp.kind == kBulkWarp && HW % W != 0 && C % 2 == 0 && C / 2 >= kSplitMinChannels &&
                    (C / 2) % G == 0 && (static_cast<int64_t>(C / 2) * HW) % 8 == 0 && bytes >= kSplitBulkMinBytes;
-        sp.S = bulk_slices(((sp.split ? C / 2 : C) + G - 1) / G, P, C, sp.smem, sp.cpl);
+        sp.S = bulk_slices(((sp.split ? C / 2 : C) + G - 1) / G, P, C, sp.smem, sp.cpl,
+                           sp.kind == kBulkWarp ? kThreads / bulkw_threads(sp.cpl) : 1);
     } else if (sp.kind == kStaged) {
         sp.G = G;
         sp.slot_bytes = slot;
