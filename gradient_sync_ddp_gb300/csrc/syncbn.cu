@@ -685,7 +685,7 @@ __global__ void __launch_bounds__(bulkw_threads(CPL)) bn_stats_bulkw_kernel(cons
         red_q[(warp * CPL + m) * 32 + lane] = acc_q[m];
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < Gc; c += kT) {
+    auto combine = [&](int c) {
         const int cps = 32 >> a.tc_log2;
         const int m = c / cps;
         const int l0 = (c % cps) << a.tc_log2;
@@ -699,6 +699,11 @@ __global__ void __launch_bounds__(bulkw_threads(CPL)) bn_stats_bulkw_kernel(cons
         a.partial[static_cast<int64_t>(c0 + c) * a.S + s] =
             failed ? make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000))
                    : make_float2(__fadd_rn(S.hi, S.lo), __fadd_rn(Q.hi, Q.lo));
+    };
+    if constexpr (kT >= kThreads) {                           // G <= kThreads: a thread per channel
+        if (threadIdx.x < Gc) combine(threadIdx.x);
+    } else {
+        for (int c = threadIdx.x; c < Gc; c += kT) combine(c);
     }
 }
 
