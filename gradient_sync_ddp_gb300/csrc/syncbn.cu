@@ -277,9 +277,10 @@ __global__ void __launch_bounds__(kThreads) bn_stats_group_kernel(const __grid_c
 // per SM: on 8 x [32, 2048, 7, 7] bf16, 4-5 runs per tile (6 CTAs per SM)
 // beat 8 runs (4 CTAs per SM) by 3 %, and 2-3 runs or two waves of CTAs
 // were slower.  Warp w sums run w of the tile; within a run, lane l owns a
-// contiguous range of one channel's plane (G >= 32: whole planes of channels
-// l, l+32, ...; G < 32: 32/G lanes split each plane), so every element it
-// reads belongs to its channel and needs no mask.  Each wait for a copy is
+// contiguous range of one channel's plane (Tc = 2^tc_log2 lanes share a
+// plane: 32/G for G < 32, up to one 16-byte vector per lane on short aligned
+// planes, else one lane per plane, for channels l, l+32, ...), so every
+// element it reads belongs to its channel and needs no mask.  Each wait for a copy is
 // bounded (about a second of globaltimer): on expiry the CTA writes NaN
 // partials for its channels, which makes the statistics NaN, instead of
 // waiting on.
@@ -547,10 +548,11 @@ __global__ void __launch_bounds__(kThreads) bn_stats_bulk_kernel(const __grid_co
 }
 
 // Bulk-staged kernel with a pipeline per warp, same grid, planes and lane
-// mapping as the tiled kernel above: warp w of the CTA owns runs w, w + 8,
-// ... of the CTA's slice and streams them through kBulkWarpRuns buffers of
-// its own, each completed on its own mbarrier, which every lane of the warp
-// waits on itself; a buffer is refilled as soon as its warp has summed it.
+// mapping as the tiled kernel above, in CTAs of bulkw_threads(CPL) threads:
+// warp w of a CTA of k warps owns runs w, w + k, ... of the CTA's slice and
+// streams them through kBulkWarpRuns buffers of its own, each completed on
+// its own mbarrier, which every lane of the warp waits on itself; a buffer
+// is refilled as soon as its warp has summed it.
 // No CTA barrier sits inside the loop, so a warp never waits for another
 // warp's copies or sums.  Used where the warps' buffers fit in
 // kBulkWarpMaxSmem (short runs: 7x7, 14x14, 8x8 bf16); measured on
